@@ -1,0 +1,16 @@
+"""CPU oracle for mask-only logits -- test infrastructure, not part of the product.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may import it.
+It shares no code with ``masked_token_lm_gb300`` and never imports it.
+"""
+from .mask_only_logits import (  # noqa: F401
+    bf16_bits_to_f64,
+    chunk_ranges,
+    f64_to_bf16_bits,
+    full_logits,
+    logits_bytes,
+    masked_logits,
+    masked_logits_chunked,
+    resolve_rows,
+    round_output,
+)
