@@ -1,0 +1,416 @@
+"""Benchmark of mask-only logits on GB300 (one JSON line on rank 0).
+
+Default workload: the LLaDA-8B-shaped LM head (one sequence L=4096, d=4096, V=126,464, bf16),
+one step = the three mask ratios r_m = 0.1, 0.5, 0.9 computed back to back (M = 410, 2048,
+3686 rows; bf16 logits [M, V]). Inputs are seeded synthetic data resident in HBM; W alone
+(1.04 GB) is larger than L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank computes its own batch (different seeds) with no collective
+on the data path; timing is the max over ranks ("weak" scaling).
+``--impl reference`` times the CPU oracle on this host's cores on a bounded sample of the same
+workload (the comparison arm; rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "masked-logits TFLOP/s (and GB/s) at 1 GB300, % of roofline"
+UNIT = "TFLOP/s"
+
+
+def workload_set(name):
+    from masked_token_lm_gb300 import workloads as wl
+
+    table = {
+        "llada8b": wl.LLADA,
+        "tiny": [wl.TINY],
+        "decode": [wl.DECODE],
+        "dream": [wl.DREAM],
+        "long": wl.LONG,
+    }
+    for w in wl.LONG + wl.LLADA:
+        table[w.name] = [w]
+    return table[name]
+
+
+def describe(name, ws):
+    w0 = ws[0]
+    return {
+        "workload": name if len(ws) > 1 else w0.name,
+        "members": [w.name for w in ws],
+        "B": w0.B, "L": w0.L, "d": w0.d, "V": w0.V,
+        "out_dtype": w0.out_dtype,
+        "chunk_rows": w0.chunk_rows,
+        "l2": "inputs larger than L2 (W alone exceeds the 129 MB L2); no flush",
+    }
+
+
+def algorithmic_bytes(M, V, d, out_elt):
+    """W once + the gathered hidden rows once + the output once (+ 4 B per index)."""
+    return 2 * V * d + 2 * M * d + out_elt * M * V + 4 * M
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return j["hbm_gbs"], j["bf16_tflops"], j.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class CpuOracleTimer:
+    """Times the CPU oracle, as it stands, on a bounded sample of a workload: the first n
+    masked rows of the middle member, all V columns. Inputs are generated once."""
+
+    def __init__(self, ws):
+        import numpy as np
+        import torch
+
+        from oracle import mask_only_logits as orc
+
+        self.orc = orc
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        self.w = w = ws[len(ws) // 2]
+        mask = w.mask()
+        self.Hb = w.hidden("cpu").view(torch.int16).numpy().view(np.uint16)
+        self.Wb = w.weight("cpu").view(torch.int16).numpy().view(np.uint16)
+        so = None if mask.seq_offsets is None else mask.seq_offsets.numpy()
+        mo = None if mask.mask_offsets is None else mask.mask_offsets.numpy()
+        self.rows = orc.resolve_rows(mask.idx.numpy(), w.L_tot, so, mo).astype(np.int32)
+        self.n = None
+
+    def calibrate(self, target_s):
+        t0 = time.perf_counter()
+        self.orc.masked_logits(self.Hb, self.rows[:8], self.Wb)
+        dt = time.perf_counter() - t0
+        self.n = int(max(8, min(len(self.rows), 8 * target_s / max(dt, 1e-3))))
+        return self.n
+
+    def run(self):
+        t0 = time.perf_counter()
+        self.orc.masked_logits(self.Hb, self.rows[:self.n], self.Wb)
+        dt = time.perf_counter() - t0
+        flops = 2 * self.n * self.w.V * self.w.d
+        return flops / dt / 1e12, dt
+
+    def sample(self):
+        return (f"oracle (bf16 decode + fp64 gather and matmul, numpy/OpenBLAS) on the first "
+                f"{self.n} masked rows of {self.w.name}, all V={self.w.V} columns; per call")
+
+
+def bench_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    ws = workload_set(args.workload)
+    timer = CpuOracleTimer(ws)
+    per_step = min(args.ref_step_s, 150.0 / max(1, args.steps + args.warmup))
+    timer.calibrate(per_step)
+    for _ in range(args.warmup):
+        timer.run()
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        v, s = timer.run()
+        vals.append(v)
+        secs += s
+    value = secs and (2 * timer.n * timer.w.V * timer.w.d * args.steps) / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(args.workload, ws),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
+                         "sample": timer.sample()},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_cuda(args):
+    import torch
+
+    from masked_token_lm_gb300 import mosaic as mz
+    from masked_token_lm_gb300 import workloads as wl
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    ws = workload_set(args.workload)
+    mo = mz.Mosaic(local)
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs resident in HBM (per-rank seeds: each rank owns an independent batch)
+    seed_shift = 100000 * rank
+    calls = []
+    tot_flops = tot_bytes = 0
+    for w in ws:
+        mask = w.mask().to(dev)
+        H = wl.make_hidden(w.L_tot, w.d, w.seed + 1 + seed_shift, dev)
+        W = wl.make_weight(w.V, w.d, w.seed + 2 + seed_shift, dev)
+        odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
+        chunked = 0 < w.chunk_rows < mask.M
+        out = torch.empty((w.chunk_rows if chunked else mask.M, w.V), dtype=odt, device=dev)
+        calls.append(dict(w=w, mask=mask, H=H, W=W, out=out, odt=odt, chunked=chunked))
+        tot_flops += w.flops(mask.M)
+        tot_bytes += algorithmic_bytes(mask.M, w.V, w.d, out.element_size())
+    # identical W across members of one workload set: share it
+    for c in calls[1:]:
+        if c["w"].V == calls[0]["w"].V and c["w"].d == calls[0]["w"].d:
+            c["W"] = calls[0]["W"]
+
+    noop = (lambda *a: None)
+
+    def one_call(c):
+        m = c["mask"]
+        mo.masked_logits(c["H"], m.idx, c["W"], m.seq_offsets, m.mask_offsets, out=c["out"],
+                         chunk_rows=c["w"].chunk_rows, on_chunk=noop if c["chunked"] else None,
+                         stream=stream)
+
+    def step():
+        for c in calls:
+            one_call(c)
+
+    for _ in range(args.warmup):
+        step()
+    st = mo.check()
+    if st != mz.MOSAIC_OK:
+        raise SystemExit(f"kernel status {st}: {mz.mosaic_last_error_string()}")
+
+    # ---- device-timed region: per-call events on the launching stream
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = mo.launches
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps * len(calls))]
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        k = 0
+        for _ in range(args.steps):
+            for c in calls:
+                evs[k][0].record(stream)
+                one_call(c)
+                evs[k][1].record(stream)
+                k += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    launches = mo.launches - launches0
+    st = mo.check()
+    if st != mz.MOSAIC_OK:
+        raise SystemExit(f"kernel status {st}: {mz.mosaic_last_error_string()}")
+    total_ms = t_start.elapsed_time(t_end)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        t = torch.tensor([total_ms, kernel_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, kernel_ms = t.tolist()
+    ms_per_step = total_ms / args.steps
+    value = world * tot_flops / (ms_per_step * 1e-3) / 1e12
+    gbs = world * tot_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the public call: pinned host inputs -> device -> logits -> host
+    e2e = None
+    if not args.no_e2e:
+        host_in, host_out = [], []
+        h2d = d2h = 0
+        for c in calls:
+            hi = {"H": c["H"].cpu().pin_memory(), "idx": c["mask"].idx.cpu().pin_memory()}
+            if c is calls[0] or c["W"] is not calls[0]["W"]:
+                hi["W"] = c["W"].cpu().pin_memory()
+            for k2 in ("so", "mo"):
+                t = c["mask"].seq_offsets if k2 == "so" else c["mask"].mask_offsets
+                if t is not None:
+                    hi[k2] = t.cpu().pin_memory()
+            host_in.append(hi)
+            h2d += sum(t.numel() * t.element_size() for t in hi.values())
+            full_rows = c["mask"].M
+            ho = torch.empty((full_rows, c["w"].V), dtype=c["odt"], pin_memory=True)
+            host_out.append(ho)
+            d2h += ho.numel() * ho.element_size()
+        dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items()} for hi in host_in]
+
+        def e2e_step():
+            Wd = None
+            for c, hi, di, ho in zip(calls, host_in, dev_in, host_out):
+                for k2, v in hi.items():
+                    di[k2].copy_(v, non_blocking=True)
+                Wd = di.get("W", Wd)
+
+                def on_chunk(ci, rb, rows, out, ho=ho):
+                    ho[rb:rb + rows].copy_(out[:rows], non_blocking=True)
+
+                mo.masked_logits(di["H"], di["idx"], Wd, di.get("so"), di.get("mo"), out=c["out"],
+                                 chunk_rows=c["w"].chunk_rows, on_chunk=on_chunk, stream=stream)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        assert mo.check() == mz.MOSAIC_OK
+        e2e = {"value": world * tot_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "steps": n_e2e}
+
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    kernel_tflops = tot_flops * args.steps / (kernel_ms * 1e-3) / 1e12
+    roof_time = max(tot_flops / (bf16 * 1e12), tot_bytes / (hbm * 1e9))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**describe(args.workload, ws),
+                   "M": [c["mask"].M for c in calls],
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "gbs": gbs,
+        "roofline_frac_of_step": roof_time / (ms_per_step * 1e-3) if world == 1 else None,
+        "roofline": {
+            "bound": "tensor" if tot_flops / (bf16 * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm",
+            "achieved": kernel_tflops, "peak": bf16, "unit": "TFLOP/s",
+            "frac": kernel_tflops / bf16, "traffic": args.traffic,
+            "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+            "kernel": "gather_gemm_kernel<false>", "achieved_gbs": tot_bytes * args.steps / (kernel_ms * 1e-3) / 1e9,
+            "hbm_peak_gbs": hbm,
+        },
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        timer = CpuOracleTimer(ws)
+        timer.calibrate(args.ref_step_s)
+        v, secs = timer.run()
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
+                                "sample": timer.sample(), "seconds": secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    mo.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llada8b")
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=15.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_cuda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,143 @@
+/*
+ * mosaic.h -- C ABI of the GB300 (sm_103a) mask-only logits library, libmosaic.so.
+ *
+ * The operation. "Mosaic: Unlocking Long-Context Inference for Diffusion LLMs via Global
+ * Memory" (paper review), section 3, observation #2 and core component 1 "Mask-only Logits
+ * Kernel": at each denoising step only the still-masked tokens are sampled, so logits are
+ * computed for those tokens alone, by one gather-GEMM launch that takes the hidden states of
+ * all tokens plus the mask indices, addresses the hidden rows indirectly through the indices
+ * and writes no intermediate gathered buffer:
+ *
+ *     out[i, v] = sum_k hidden[row(i), k] * W[v, k]        0 <= i < M, 0 <= v < V
+ *
+ * with fp32 accumulation and bf16 (round-to-nearest-even) or fp32 output. Lazy chunking
+ * ("扩散大语言模型内存优化：Mosaic系统突破与实践", section 2.3; dLLM-Serve article
+ * "扩散大语言模型内存优化：从理论到系统设计", section 3.2.2): when a chunk size is given and
+ * M exceeds it, consecutive row slices are computed one after another into the same output
+ * buffer, and the concatenation of the slices equals the unchunked result bit for bit.
+ *
+ * Conventions for every call below:
+ *   - All array pointers are DEVICE pointers on the handle's device unless stated otherwise;
+ *     the caller allocates and owns them. The library allocates nothing per call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *     default stream). Argument errors are detected on the host and returned before anything
+ *     is enqueued. Errors seen by the GPU (bad indices, a wait that ran out) are recorded in
+ *     the handle's device status word and reported by mosaic_check().
+ *   - Not thread-safe per handle: one host thread per handle at a time.
+ */
+#ifndef MOSAIC_H_
+#define MOSAIC_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOSAIC_API __attribute__((visibility("default")))
+#else
+#define MOSAIC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOSAIC_OK = 0,
+  MOSAIC_ERR_INVALID_ARG = 1, /* host-detected bad argument; nothing was enqueued          */
+  MOSAIC_ERR_UNSUPPORTED = 2, /* shape/alignment/device outside what the kernel handles    */
+  MOSAIC_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                         */
+  MOSAIC_ERR_INDEX = 4,       /* (mosaic_check) a mask index fell outside its sequence / H */
+  MOSAIC_ERR_TIMEOUT = 5      /* (mosaic_check) a bounded on-GPU wait ran out              */
+} mosaic_status;
+
+typedef enum { MOSAIC_BF16 = 0, MOSAIC_F32 = 1 } mosaic_dtype;
+
+typedef struct mosaic_handle mosaic_handle;
+
+/*
+ * Called on the host after chunk `chunk` has been enqueued on the stream (see
+ * mosaic_masked_logits). `out` holds rows [row_begin, row_begin + rows) of the result once
+ * the stream reaches this point; the consumer must enqueue its work on the same stream (or
+ * otherwise order it before the next chunk) because the next chunk overwrites `out`.
+ */
+typedef void (*mosaic_chunk_cb)(int64_t chunk, int64_t row_begin, int64_t rows, void* out,
+                                void* user);
+
+/*
+ * Create a handle bound to CUDA device `device` (made current by this call). The handle owns
+ * one small device status word and the device properties used for launch sizing. Returns
+ * MOSAIC_ERR_UNSUPPORTED on a device that is not sm_103, MOSAIC_ERR_CUDA if CUDA fails.
+ */
+MOSAIC_API mosaic_status mosaic_create(mosaic_handle** handle, int device);
+
+/* Free the handle (synchronises the device first). NULL is accepted. */
+MOSAIC_API mosaic_status mosaic_destroy(mosaic_handle* handle);
+
+/*
+ * Mask-only logits (gather-GEMM), one persistent kernel launch per chunk.
+ *
+ * hidden        bf16 [L_tot, d], row-major, row stride d elements; 16-byte aligned.
+ * mask_idx      int32 [M]. Flat mode (seq_offsets == mask_offsets == NULL): global rows of
+ *               hidden. CSR mode: positions local to their sequence (see below). Any order,
+ *               duplicates allowed; output row i always belongs to mask_idx[i].
+ * seq_offsets   CSR mode: int32 [B+1], rising; sequence b owns hidden rows
+ *               [seq_offsets[b], seq_offsets[b+1]), seq_offsets[B] <= L_tot.
+ * mask_offsets  CSR mode: int32 [B+1], rising from 0 to M; sequence b owns
+ *               mask_idx[mask_offsets[b] .. mask_offsets[b+1]), and the hidden row of such an
+ *               entry is seq_offsets[b] + mask_idx[i].
+ * B             number of sequences in CSR mode (>= 1), ignored in flat mode.
+ * W             bf16 [V, d] LM-head weight, row-major; 16-byte aligned.
+ * out           [rows_out, V] row-major in out_dtype, 16-byte aligned, where
+ *               rows_out = M if chunking is off, else chunk_rows.
+ * chunk_rows    <= 0 or >= M: chunking off, one launch writes out[M, V]. Otherwise rows are
+ *               cut into slices [c*chunk_rows, min(M, (c+1)*chunk_rows)) of the flat index list
+ *               (crossing sequence boundaries in CSR mode); each slice is written to out[0..]
+ *               and then cb(c, row_begin, rows, out, user) runs on the host. cb is required
+ *               when chunking is on; when chunking is off a non-NULL cb runs once (c = 0).
+ * stream        cudaStream_t (as void*) to enqueue on.
+ *
+ * Requirements (else MOSAIC_ERR_INVALID_ARG / MOSAIC_ERR_UNSUPPORTED, nothing enqueued):
+ * non-NULL pointers (except the CSR pair in flat mode, cb when unchunked), d % 8 == 0,
+ * V % 8 == 0, 1 <= d, 1 <= V, 0 <= M, L_tot < 2^31, M < 2^31, both CSR arrays or neither.
+ * M == 0 returns MOSAIC_OK without launching or calling cb; the array pointers are then
+ * not looked at and may be NULL.
+ *
+ * Bad indices are not an argument error (the host cannot read them): an index outside its
+ * sequence or outside hidden makes that output row all zeros and sets the status word, which
+ * mosaic_check() reports as MOSAIC_ERR_INDEX. The same holds for CSR offsets that do not
+ * start at 0 and end at M.
+ */
+MOSAIC_API mosaic_status mosaic_masked_logits(mosaic_handle* handle,
+                                              const void* hidden, int64_t L_tot, int64_t d,
+                                              const int32_t* mask_idx, int64_t M,
+                                              const int32_t* seq_offsets,
+                                              const int32_t* mask_offsets, int32_t B,
+                                              const void* W, int64_t V,
+                                              void* out, mosaic_dtype out_dtype,
+                                              int64_t chunk_rows, mosaic_chunk_cb cb,
+                                              void* user, void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the handle's device status word. Returns MOSAIC_OK,
+ * MOSAIC_ERR_INDEX (a bad mask index / CSR offsets were seen), MOSAIC_ERR_TIMEOUT (a bounded
+ * wait inside a kernel gave up; the kernel returned and the CUDA context stays usable) or
+ * MOSAIC_ERR_CUDA.
+ */
+MOSAIC_API mosaic_status mosaic_check(mosaic_handle* handle, void* stream);
+
+/*
+ * Upper bound, in nanoseconds, on any single wait inside the kernel before it gives up with
+ * MOSAIC_ERR_TIMEOUT (default 2e9). Tests set a tiny value to exercise the timeout path.
+ */
+MOSAIC_API mosaic_status mosaic_set_wait_timeout(mosaic_handle* handle, uint64_t timeout_ns);
+
+/* Number of kernel launches enqueued through this handle since creation. */
+MOSAIC_API int64_t mosaic_launch_count(const mosaic_handle* handle);
+
+/* Text of the last error produced on the calling thread ("" if none). */
+MOSAIC_API const char* mosaic_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOSAIC_H_ */

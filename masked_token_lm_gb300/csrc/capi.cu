@@ -1,0 +1,257 @@
+// C ABI of libmosaic.so: argument validation, TMA descriptor set-up and the lazy-chunk driver
+// around the gather-GEMM kernel. The declarations and their contracts are in include/mosaic.h.
+//
+// Lazy chunking follows "扩散大语言模型内存优化：Mosaic系统突破与实践" (section 2.3: chunking is
+// off by default and used only when asked for) and the dLLM-Serve article
+// "扩散大语言模型内存优化：从理论到系统设计" (section 3.2.2: rows beyond the cap are cut into
+// consecutive slices, each run through the LM head). Here every slice reuses one output buffer
+// and the kernel's per-element arithmetic does not depend on where a row falls in a slice, so
+// the concatenated slices equal the unchunked result bit for bit.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/mosaic.h"
+#include "gather_gemm.h"
+
+struct mosaic_handle {
+  int device = 0;
+  int num_sms = 0;
+  uint32_t* d_status = nullptr;
+  uint64_t timeout_ns = 2000000000ull;
+  int64_t launches = 0;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mosaic_status fail(mosaic_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+mosaic_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOSAIC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device memory the handle's GPU can address (device or managed allocation).
+bool is_device_ptr(const void* p, int device) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice) return a.device == device;
+  return a.type == cudaMemoryTypeManaged;
+}
+
+// 2-D row-major tensor [rows, cols] of `elt`-byte elements, box {box_cols, box_rows}, 128-byte
+// swizzle (box_cols * elt == 128), zero fill outside the tensor.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* base,
+               uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * elt};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// M tiles per raster group: as many as keep the group's gathered rows (BM x d bf16 each)
+// within ~48 MiB of L2, so that W panels are streamed once per group.
+int pick_group_m(int m_tiles, int64_t d) {
+  const int64_t per_tile = static_cast<int64_t>(mosaic::gather_gemm_block_m()) * d * 2;
+  int64_t g = (48ll << 20) / per_tile;
+  if (g < 1) g = 1;
+  if (g > m_tiles) g = m_tiles;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mosaic_last_error_string(void) { return g_last_error.c_str(); }
+
+mosaic_status mosaic_create(mosaic_handle** handle, int device) {
+  if (!handle) return fail(MOSAIC_ERR_INVALID_ARG, "handle out-pointer is NULL");
+  *handle = nullptr;
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(MOSAIC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                device, prop.major, prop.minor);
+  if (!encode_fn()) return fail(MOSAIC_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  for (bool f32 : {false, true}) {
+    e = mosaic::gather_gemm_prepare(f32);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  auto* h = new mosaic_handle();
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  e = cudaMalloc(&h->d_status, 256);
+  if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 256);
+  if (e != cudaSuccess) {
+    if (h->d_status) cudaFree(h->d_status);
+    delete h;
+    return cuda_fail(e, "status word allocation");
+  }
+  *handle = h;
+  g_last_error.clear();
+  return MOSAIC_OK;
+}
+
+mosaic_status mosaic_destroy(mosaic_handle* h) {
+  if (!h) return MOSAIC_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->d_status);
+  delete h;
+  return MOSAIC_OK;
+}
+
+mosaic_status mosaic_set_wait_timeout(mosaic_handle* h, uint64_t timeout_ns) {
+  if (!h) return fail(MOSAIC_ERR_INVALID_ARG, "NULL handle");
+  h->timeout_ns = timeout_ns;
+  return MOSAIC_OK;
+}
+
+int64_t mosaic_launch_count(const mosaic_handle* h) { return h ? h->launches : -1; }
+
+mosaic_status mosaic_check(mosaic_handle* h, void* stream) {
+  if (!h) return fail(MOSAIC_ERR_INVALID_ARG, "NULL handle");
+  cudaSetDevice(h->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, h->d_status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  e = cudaMemset(h->d_status, 0, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  if (word & mosaic::MOSAIC_STATUS_TIMEOUT)
+    return fail(MOSAIC_ERR_TIMEOUT, "a bounded wait inside the kernel ran out");
+  if (word & mosaic::MOSAIC_STATUS_INDEX)
+    return fail(MOSAIC_ERR_INDEX, "a mask index (or CSR offset) was outside its sequence");
+  return MOSAIC_OK;
+}
+
+mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t L_tot,
+                                   int64_t d, const int32_t* mask_idx, int64_t M,
+                                   const int32_t* seq_offsets, const int32_t* mask_offsets,
+                                   int32_t B, const void* W, int64_t V, void* out,
+                                   mosaic_dtype out_dtype, int64_t chunk_rows,
+                                   mosaic_chunk_cb cb, void* user, void* stream_ptr) {
+  if (!h) return fail(MOSAIC_ERR_INVALID_ARG, "NULL handle");
+  if (M < 0) return fail(MOSAIC_ERR_INVALID_ARG, "M < 0");
+  if (M >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "M >= 2^31");
+  if (out_dtype != MOSAIC_BF16 && out_dtype != MOSAIC_F32)
+    return fail(MOSAIC_ERR_INVALID_ARG, "unknown out_dtype %d", static_cast<int>(out_dtype));
+  if ((seq_offsets == nullptr) != (mask_offsets == nullptr))
+    return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs both seq_offsets and mask_offsets");
+  const bool csr = seq_offsets != nullptr;
+  if (csr && B < 1) return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs B >= 1");
+  const bool chunked = chunk_rows > 0 && chunk_rows < M;
+  if (chunked && !cb) return fail(MOSAIC_ERR_INVALID_ARG, "chunking on (chunk_rows < M) needs a callback");
+  if (M == 0) return MOSAIC_OK;  // nothing to read or write: no launch, no callback
+  if (!hidden || !W || !out || !mask_idx)
+    return fail(MOSAIC_ERR_INVALID_ARG, "NULL hidden, W, out or mask_idx");
+  if (d < 1 || V < 1 || L_tot < 1) return fail(MOSAIC_ERR_INVALID_ARG, "d, V and L_tot must be >= 1");
+  if (d % 8 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 8 (16-byte rows)");
+  if (V % 8 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "V must be a multiple of 8 (16-byte rows)");
+  if (L_tot >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "L_tot >= 2^31");
+  if (V >= (1ll << 31) || d >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "V or d too large");
+  if (!aligned16(hidden) || !aligned16(W) || !aligned16(out))
+    return fail(MOSAIC_ERR_INVALID_ARG, "hidden, W and out must be 16-byte aligned");
+
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  if (!is_device_ptr(hidden, h->device) || !is_device_ptr(W, h->device) ||
+      !is_device_ptr(out, h->device) || !is_device_ptr(mask_idx, h->device) ||
+      (csr && (!is_device_ptr(seq_offsets, h->device) || !is_device_ptr(mask_offsets, h->device))))
+    return fail(MOSAIC_ERR_INVALID_ARG, "every array must be device memory of device %d", h->device);
+
+  const bool f32 = out_dtype == MOSAIC_F32;
+  const int BM = mosaic::gather_gemm_block_m(), BN = mosaic::gather_gemm_block_n(),
+            BK = mosaic::gather_gemm_block_k();
+  const int64_t cr = chunked ? chunk_rows : M;
+  const int64_t n_tiles = (V + BN - 1) / BN;
+  const int64_t m_tiles_max = (cr + BM - 1) / BM;
+  if (m_tiles_max * n_tiles >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "too many tiles");
+
+  CUtensorMap tm_h, tm_w, tm_out;
+  if (!encode_2d(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hidden, L_tot, d, 1, BK))
+    return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for hidden rejected");
+  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d, BN, BK))
+    return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t n_chunks = (M + cr - 1) / cr;
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t rb = c * cr;
+    const int64_t rows = (M - rb < cr) ? (M - rb) : cr;
+    const CUtensorMapDataType odt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_2d(&tm_out, odt, f32 ? 4 : 2, out, rows, V, BM, mosaic::gather_gemm_epi_cols(f32)))
+      return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for out rejected");
+    mosaic::GatherGemmParams p;
+    p.idx = mask_idx;
+    p.seq_offsets = csr ? seq_offsets : nullptr;
+    p.mask_offsets = csr ? mask_offsets : nullptr;
+    p.L_tot = L_tot;
+    p.B = csr ? B : 0;
+    p.M_total = static_cast<int32_t>(M);
+    p.row_begin = static_cast<int32_t>(rb);
+    p.rows = static_cast<int32_t>(rows);
+    p.chunk_index = static_cast<int32_t>(c);
+    p.V = static_cast<int32_t>(V);
+    p.k_blocks = static_cast<int32_t>((d + BK - 1) / BK);
+    p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
+    p.n_tiles = static_cast<int32_t>(n_tiles);
+    p.group_m = pick_group_m(p.m_tiles, d);
+    p.status = h->d_status;
+    p.timeout_ns = h->timeout_ns;
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    e = mosaic::gather_gemm_launch(tm_h, tm_w, tm_out, p, f32, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
+    ++h->launches;
+    if (cb) cb(c, rb, rows, out, user);
+  }
+  return MOSAIC_OK;
+}
+
+}  // extern "C"

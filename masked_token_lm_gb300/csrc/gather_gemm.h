@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI host layer and the gather-GEMM kernel.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mosaic {
+
+// Bits of the device status word.
+constexpr uint32_t MOSAIC_STATUS_INDEX = 1u;    // a mask index / CSR offset was out of range
+constexpr uint32_t MOSAIC_STATUS_TIMEOUT = 2u;  // a bounded wait gave up
+
+struct GatherGemmParams {
+  const int32_t* idx;           // [M_total] mask indices (whole list, not just this chunk)
+  const int32_t* seq_offsets;   // CSR [B+1] or nullptr
+  const int32_t* mask_offsets;  // CSR [B+1] or nullptr
+  int64_t L_tot;                // rows of H
+  int32_t B;                    // sequences (CSR mode)
+  int32_t M_total;              // all masked positions
+  int32_t row_begin;            // first flat position of this chunk
+  int32_t rows;                 // positions in this chunk
+  int32_t chunk_index;
+  int32_t V;
+  int32_t k_blocks;             // ceil(d / BK)
+  int32_t m_tiles, n_tiles;     // ceil(rows / BM), ceil(V / BN)
+  int32_t group_m;              // M tiles per raster group
+  uint32_t* status;             // device status word
+  uint64_t timeout_ns;          // bound on any single wait
+};
+
+int gather_gemm_smem_bytes();
+int gather_gemm_block_m();
+int gather_gemm_block_n();
+int gather_gemm_block_k();
+int gather_gemm_epi_cols(bool out_f32);
+cudaError_t gather_gemm_prepare(bool out_f32);
+cudaError_t gather_gemm_launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                               const CUtensorMap& tm_out, const GatherGemmParams& p,
+                               bool out_f32, int grid, cudaStream_t stream);
+
+}  // namespace mosaic

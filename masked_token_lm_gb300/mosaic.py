@@ -1,0 +1,195 @@
+"""Python binding of libmosaic.so (ctypes). Argument marshalling only: every step of the
+mask-only logits path runs in the library's CUDA kernels.
+
+The ``mosaic_*`` functions mirror the C ABI in ``include/mosaic.h`` one to one (raw pointers,
+integer status). ``Mosaic`` is a small convenience wrapper that takes torch tensors (torch is
+used for device memory and streams only) and raises ``MosaicError`` on a non-OK status.
+
+There is no CPU fallback: if the library is missing or no sm_103 GPU is present, the calls
+fail loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Callable, Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libmosaic.so")
+
+MOSAIC_OK = 0
+MOSAIC_ERR_INVALID_ARG = 1
+MOSAIC_ERR_UNSUPPORTED = 2
+MOSAIC_ERR_CUDA = 3
+MOSAIC_ERR_INDEX = 4
+MOSAIC_ERR_TIMEOUT = 5
+STATUS_NAMES = {0: "MOSAIC_OK", 1: "MOSAIC_ERR_INVALID_ARG", 2: "MOSAIC_ERR_UNSUPPORTED",
+                3: "MOSAIC_ERR_CUDA", 4: "MOSAIC_ERR_INDEX", 5: "MOSAIC_ERR_TIMEOUT"}
+
+MOSAIC_BF16 = 0
+MOSAIC_F32 = 1
+
+mosaic_chunk_cb = ctypes.CFUNCTYPE(None, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_void_p)
+
+_lib = None
+
+
+class MosaicError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmosaic.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m masked_token_lm_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    lib.mosaic_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+    lib.mosaic_create.restype = ctypes.c_int
+    lib.mosaic_destroy.argtypes = [P]
+    lib.mosaic_destroy.restype = ctypes.c_int
+    lib.mosaic_masked_logits.argtypes = [P, P, I64, I64, P, I64, P, P, I32, P, I64, P,
+                                         ctypes.c_int, I64, mosaic_chunk_cb, P, P]
+    lib.mosaic_masked_logits.restype = ctypes.c_int
+    lib.mosaic_check.argtypes = [P, P]
+    lib.mosaic_check.restype = ctypes.c_int
+    lib.mosaic_set_wait_timeout.argtypes = [P, ctypes.c_uint64]
+    lib.mosaic_set_wait_timeout.restype = ctypes.c_int
+    lib.mosaic_launch_count.argtypes = [P]
+    lib.mosaic_launch_count.restype = ctypes.c_int64
+    lib.mosaic_last_error_string.argtypes = []
+    lib.mosaic_last_error_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ C-ABI mirrors (same names)
+
+def mosaic_create(device: int = 0):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    st = load_library().mosaic_create(ctypes.byref(h), int(device))
+    return st, h
+
+
+def mosaic_destroy(handle) -> int:
+    return load_library().mosaic_destroy(handle)
+
+
+def mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B,
+                         W, V, out, out_dtype, chunk_rows, cb, user, stream) -> int:
+    """Raw call; pointer arguments are ints (device addresses) or None."""
+    cb_c = cb if isinstance(cb, mosaic_chunk_cb) else (mosaic_chunk_cb(cb) if cb else mosaic_chunk_cb())
+    return load_library().mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets,
+                                               mask_offsets, B, W, V, out, out_dtype, chunk_rows,
+                                               cb_c, user, stream)
+
+
+def mosaic_check(handle, stream) -> int:
+    return load_library().mosaic_check(handle, stream)
+
+
+def mosaic_set_wait_timeout(handle, timeout_ns: int) -> int:
+    return load_library().mosaic_set_wait_timeout(handle, int(timeout_ns))
+
+
+def mosaic_launch_count(handle) -> int:
+    return load_library().mosaic_launch_count(handle)
+
+
+def mosaic_last_error_string() -> str:
+    return load_library().mosaic_last_error_string().decode()
+
+
+# ------------------------------------------------------------------ torch convenience wrapper
+
+class Mosaic:
+    """Owns a handle on one CUDA device; takes torch tensors."""
+
+    def __init__(self, device: int = 0):
+        import torch  # noqa: F401  (device memory and streams)
+
+        st, h = mosaic_create(device)
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        self.handle = h
+        self.device = device
+
+    def close(self):
+        if self.handle:
+            mosaic_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _stream_ptr(stream):
+        import torch
+
+        s = stream if stream is not None else torch.cuda.current_stream()
+        return s.cuda_stream
+
+    def masked_logits(self, hidden, mask_idx, W, seq_offsets=None, mask_offsets=None,
+                      out=None, out_dtype=None, chunk_rows: int = 0,
+                      on_chunk: Optional[Callable] = None, stream=None):
+        """Mask-only logits. Returns ``out`` ([M, V], or [chunk_rows, V] holding the last chunk
+        when chunking is on). ``on_chunk(chunk, row_begin, rows, out)`` runs on the host after
+        each chunk is enqueued; it must enqueue its use of ``out`` on the same stream."""
+        import torch
+
+        for name, t, dt in (("hidden", hidden, torch.bfloat16), ("W", W, torch.bfloat16),
+                            ("mask_idx", mask_idx, torch.int32),
+                            ("seq_offsets", seq_offsets, torch.int32),
+                            ("mask_offsets", mask_offsets, torch.int32)):
+            if t is None:
+                continue
+            if t.dtype != dt or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {dt} tensor")
+        if hidden.dim() != 2 or W.dim() != 2 or hidden.shape[1] != W.shape[1]:
+            raise ValueError("hidden [L_tot, d] and W [V, d] must agree on d")
+        M = int(mask_idx.numel())
+        V, d = int(W.shape[0]), int(W.shape[1])
+        if out_dtype is None:
+            out_dtype = out.dtype if out is not None else torch.bfloat16
+        code = {torch.bfloat16: MOSAIC_BF16, torch.float32: MOSAIC_F32}[out_dtype]
+        chunked = 0 < chunk_rows < M
+        rows_out = chunk_rows if chunked else M
+        if out is None:
+            out = torch.empty((rows_out, V), dtype=out_dtype, device=W.device)
+        csr = seq_offsets is not None
+        B = int(seq_offsets.numel()) - 1 if csr else 0
+
+        def _cb(c, rb, rows, _ptr, _user):
+            on_chunk(int(c), int(rb), int(rows), out)
+
+        cb = mosaic_chunk_cb(_cb) if on_chunk is not None else mosaic_chunk_cb()
+        st = mosaic_masked_logits(
+            self.handle, hidden.data_ptr(), int(hidden.shape[0]), d,
+            mask_idx.data_ptr() if M > 0 else None, M,
+            seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None, B,
+            W.data_ptr(), V, out.data_ptr(), code, int(chunk_rows), cb, None,
+            self._stream_ptr(stream))
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        return out
+
+    def check(self, stream=None) -> int:
+        """Synchronise and return the device status (MOSAIC_OK / _INDEX / _TIMEOUT / _CUDA)."""
+        return mosaic_check(self.handle, self._stream_ptr(stream))
+
+    def set_wait_timeout(self, ns: int):
+        mosaic_set_wait_timeout(self.handle, ns)
+
+    @property
+    def launches(self) -> int:
+        return mosaic_launch_count(self.handle)

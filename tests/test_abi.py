@@ -1,0 +1,81 @@
+"""CPU-side checks of the C-ABI library: it builds for sm_103a, loads without a GPU, exports
+exactly the functions include/mosaic.h declares, and the binding agrees with the header's
+status codes. No compute call is made here (that needs a GB300)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from masked_token_lm_gb300 import build as mbuild
+from masked_token_lm_gb300 import mosaic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mosaic.h")
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    if not os.path.exists(mbuild.LIB):
+        mbuild.build()
+    return mbuild.LIB
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOSAIC_API\s+[\w\s\*]+?\b(mosaic_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    assert declared_functions() == sorted([
+        "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
+        "mosaic_launch_count", "mosaic_masked_logits", "mosaic_set_wait_timeout"])
+
+
+def test_library_loads_and_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True).stdout
+    exported = sorted(set(re.findall(r" T (mosaic_\w+)", out)))
+    assert exported == declared_functions()
+
+
+def test_status_codes_match_header():
+    text = open(HEADER).read()
+    for name, val in re.findall(r"(MOSAIC_(?:OK|ERR_\w+))\s*=\s*(\d+)", text):
+        assert getattr(mosaic, name) == int(val), name
+    for name, val in re.findall(r"(MOSAIC_(?:BF16|F32))\s*=\s*(\d+)", text):
+        assert getattr(mosaic, name) == int(val), name
+
+
+def test_null_handle_is_rejected_without_a_gpu(lib_path):
+    mosaic.load_library()
+    st = mosaic.mosaic_masked_logits(None, None, 1, 8, None, 0, None, None, 0, None, 8, None,
+                                     0, 0, None, None, None)
+    assert st == mosaic.MOSAIC_ERR_INVALID_ARG
+    assert "handle" in mosaic.mosaic_last_error_string()
+    assert mosaic.mosaic_check(None, None) == mosaic.MOSAIC_ERR_INVALID_ARG
+    assert mosaic.mosaic_launch_count(None) == -1
+    assert mosaic.mosaic_destroy(None) == mosaic.MOSAIC_OK
+
+
+def test_create_without_gpu_fails_cleanly(lib_path):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, h = mosaic.mosaic_create(0)
+    assert st in (mosaic.MOSAIC_ERR_CUDA, mosaic.MOSAIC_ERR_UNSUPPORTED)
+    assert not h.value
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "masked_token_lm_gb300")
+    for dp, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dp, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from\s+oracle|import\s+oracle)", src, re.M), f
+                assert not re.search(r'#include\s+"[^"]*oracle', src), f

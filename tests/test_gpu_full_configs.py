@@ -1,0 +1,96 @@
+"""GPU parity at the full workload sizes, in the launch configuration the benchmark times.
+
+Too large for the oracle to check every element, so each check is one of:
+* sampled rows (all V columns) plus every row on a seeded slice of columns, against the oracle;
+* lazy chunking: the chunked call (the workload's chunk_rows) equals the unchunked call bitwise;
+* one-hot hidden states: out[i, v] == W[v, row(i) mod d] exactly, for every element.
+"""
+import numpy as np
+import pytest
+import torch
+
+from masked_token_lm_gb300 import mosaic as mz
+from masked_token_lm_gb300 import workloads as wl
+from tests.parity_utils import bits, column_parity, oracle_rows, sampled_parity
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def mo():
+    m = mz.Mosaic(0)
+    yield m
+    m.close()
+
+
+def call(mo, w, H, mask, W, chunk_rows):
+    """Run one workload; returns the full [M, V] output (chunks copied out on-stream)."""
+    odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
+    M = mask.M
+    if 0 < chunk_rows < M:
+        full = torch.empty((M, w.V), dtype=odt, device=DEV)
+
+        def on_chunk(c, rb, rows, out):
+            full[rb:rb + rows].copy_(out[:rows])
+
+        mo.masked_logits(H, mask.idx, W, mask.seq_offsets, mask.mask_offsets, out_dtype=odt,
+                         chunk_rows=chunk_rows, on_chunk=on_chunk)
+        out = full
+    else:
+        out = mo.masked_logits(H, mask.idx, W, mask.seq_offsets, mask.mask_offsets, out_dtype=odt)
+    assert mo.check() == mz.MOSAIC_OK, mz.mosaic_last_error_string()
+    return out
+
+
+def check_against_oracle(w, H, mask, W, out, seed):
+    Hb, Wb = bits(H), bits(W)
+    rows = oracle_rows(mask, w.L_tot)
+    must = []
+    if w.chunk_rows:
+        for b in range(0, mask.M, w.chunk_rows):
+            must += [b, min(mask.M, b + w.chunk_rows) - 1]
+    sampled_parity(Hb, Wb, rows, lambda ri: out[torch.from_numpy(ri).to(DEV)], torch.bfloat16
+                   if w.out_dtype == "bf16" else torch.float32, seed, must_rows=must)
+    column_parity(Hb, Wb, rows, lambda cols: out[:, torch.from_numpy(cols).to(DEV)],
+                  torch.bfloat16 if w.out_dtype == "bf16" else torch.float32, seed)
+
+
+@pytest.mark.parametrize("w", wl.LLADA + [wl.DECODE], ids=lambda w: w.name)
+def test_unchunked_configs_sampled_parity(mo, w):
+    H, W, mask = w.hidden(DEV), w.weight(DEV), w.mask().to(DEV)
+    out = call(mo, w, H, mask, W, w.chunk_rows)
+    check_against_oracle(w, H, mask, W, out, seed=w.seed)
+
+
+@pytest.mark.parametrize("w", [wl.LONG[0], wl.LONG[3], wl.DREAM], ids=lambda w: w.name)
+def test_chunked_configs_equal_unchunked_and_oracle(mo, w):
+    H, W, mask = w.hidden(DEV), w.weight(DEV), w.mask().to(DEV)
+    chunked = call(mo, w, H, mask, W, w.chunk_rows)
+    whole = call(mo, w, H, mask, W, 0)
+    assert torch.equal(chunked.view(torch.int16), whole.view(torch.int16))
+    del whole
+    check_against_oracle(w, H, mask, W, chunked, seed=w.seed)
+
+
+def test_long_config_middle_ratios_chunked_equal_unchunked(mo):
+    for w in wl.LONG[1:3]:
+        H, W, mask = w.hidden(DEV), w.weight(DEV), w.mask().to(DEV)
+        chunked = call(mo, w, H, mask, W, w.chunk_rows)
+        whole = call(mo, w, H, mask, W, 0)
+        assert torch.equal(chunked.view(torch.int16), whole.view(torch.int16)), w.name
+        del chunked, whole
+
+
+@pytest.mark.parametrize("w", [wl.DECODE, wl.DREAM], ids=lambda w: w.name)
+def test_one_hot_full_size_is_bit_exact(mo, w):
+    # H[r, :] = e_(r mod d) at the workload's full shape: every output element is one weight.
+    r = torch.arange(w.L_tot, device=DEV)
+    H = torch.zeros((w.L_tot, w.d), dtype=torch.bfloat16, device=DEV)
+    H[r, r % w.d] = 1.0
+    W = w.weight(DEV)
+    m = w.mask()
+    rows = torch.from_numpy(oracle_rows(m, w.L_tot)).to(DEV)
+    out = call(mo, w, H, m.to(DEV), W, w.chunk_rows)
+    want = W.t()[rows % w.d]  # [M, V]: row i is column (row(i) mod d) of W
+    assert torch.equal(out.view(torch.int16), want.contiguous().view(torch.int16))
