@@ -213,9 +213,7 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
   const int64_t m_tiles_max = (cr + BM - 1) / BM;
   if (m_tiles_max * n_tiles >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "too many tiles");
 
-  CUtensorMap tm_h, tm_w, tm_out;
-  if (!encode_2d(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hidden, L_tot, d, 1, BK))
-    return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for hidden rejected");
+  CUtensorMap tm_w, tm_out;
   if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d, BN, BK))
     return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
 
@@ -228,6 +226,7 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     if (!encode_2d(&tm_out, odt, f32 ? 4 : 2, out, rows, V, BM, mosaic::gather_gemm_epi_cols(f32)))
       return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for out rejected");
     mosaic::GatherGemmParams p;
+    p.hidden = hidden;
     p.idx = mask_idx;
     p.seq_offsets = csr ? seq_offsets : nullptr;
     p.mask_offsets = csr ? mask_offsets : nullptr;
@@ -238,6 +237,7 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     p.rows = static_cast<int32_t>(rows);
     p.chunk_index = static_cast<int32_t>(c);
     p.V = static_cast<int32_t>(V);
+    p.d = static_cast<int32_t>(d);
     p.k_blocks = static_cast<int32_t>((d + BK - 1) / BK);
     p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
     p.n_tiles = static_cast<int32_t>(n_tiles);
@@ -246,7 +246,7 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     p.timeout_ns = h->timeout_ns;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
-    e = mosaic::gather_gemm_launch(tm_h, tm_w, tm_out, p, f32, grid, stream);
+    e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     ++h->launches;
     if (cb) cb(c, rb, rows, out, user);

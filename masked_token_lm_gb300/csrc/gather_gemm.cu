@@ -9,14 +9,20 @@
 // buffer is ever written. The pages' kernel targeted RTX 3090 / A100; this one is designed for
 // Blackwell instead:
 //
-//   warp 0      producer: resolves the tile's 128 mask indices to hidden rows (index staging),
-//               then per K block issues 32 TMA gather4 row loads for A (4 rows each) and one
-//               2-D TMA load for the W tile into a STAGES-deep shared-memory ring.
+//   warps 6..9  A gather: each of the 128 threads resolves 8 of the tile's mask indices to
+//               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
+//               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
+//               a STAGES-deep shared-memory ring (8 threads cover one 128-byte row segment).
+//   warp 0      W stream: one thread issues a 2-D TMA load of the 256 x 64 W tile per K block.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16) into a
 //               double-buffered TMEM accumulator (2 x 256 columns) and commits stage releases.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator, round to bf16 (or keep fp32), write
 //               128-byte-swizzled staging tiles and TMA-store them; rows past the chunk are
 //               clipped by the store's tensor map.
+//
+// The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
+// 32 gather4 instructions a 128-row K block needs held the kernel to ~26 % of the tensor peak,
+// while the same bytes through the load/store units keep the tensor pipe fed.
 //
 // Tiles are walked by a static persistent schedule: within a group of M tiles, N panels outer
 // and M tiles inner, so each W panel is fetched from HBM once per group while the gathered A
@@ -46,9 +52,12 @@ constexpr int B_STAGE = BN * BK * 2;  // 32 KiB
 constexpr int EPI_BUF = BM * 128;     // 128 rows x 128 B
 constexpr int EPI_BUFS = 2;
 constexpr int TMEM_COLS = 2 * BN;     // two accumulators
-constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
+constexpr int A_WARP0 = 6;
+constexpr int A_THREADS = 128;
+constexpr int NUM_THREADS = (A_WARP0 * 32) + A_THREADS;  // 320
+constexpr int A_LAG = STAGES - 1;  // K blocks a gather thread keeps in flight before publishing
 
 constexpr int SMEM_A_OFF = 0;
 constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE;
@@ -157,8 +166,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const GatherGemmParams& p
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_h,
-                       const __grid_constant__ CUtensorMap tm_w,
+    gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_out,
                        const GatherGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(sm.full(s), 1);   // producer's arrive.expect_tx; bytes complete it
+      mbar_init(sm.full(s), 1 + A_THREADS);  // W arrive.expect_tx + every gather thread
       mbar_init(sm.empty(s), 1);  // MMA commit
     }
     for (int j = 0; j < 2; ++j) {
@@ -188,7 +196,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_h);
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_out);
   }
@@ -199,47 +206,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *sm.tmem_slot();
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer (TMA)
-    const uint64_t pol_w = policy_evict_normal();
-    const uint64_t pol_a = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
-    int64_t issued = 0;  // K blocks issued (for the drain after an abort)
+    // ---------------------------------------------------------------- W stream (TMA)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;  // K blocks issued (for the drain after an abort)
+      bool alive = true;
+      for (int t = blockIdx.x; t < num_tiles && alive; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, p);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
+          mbar_arrive_expect_tx(sm.full(stage), B_STAGE);
+          tma_load_2d(sm.b(stage), &tm_w, kb * BK, tc.n * BN, sm.full(stage), pol_w);
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!alive) {
+        // Let every W load already issued land before the CTA can exit.
+        for (int s = 0; s < STAGES; ++s) {
+          const int64_t last = issued - 1 - ((issued - 1 - s) % STAGES + STAGES) % STAGES;
+          if (issued > 0 && last >= 0)
+            drain_wait(sm.full(s), static_cast<uint32_t>((last / STAGES) & 1));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= A_WARP0) {
+    // ---------------------------------------------------------------- A gather (cp.async)
+    const int at = threadIdx.x - A_WARP0 * 32;  // 0..127
+    const int chunk = at & 7;                   // 16-byte piece of a 128-byte row segment
+    const int row0 = at >> 3;                   // this thread's rows: row0 + 16 j, j = 0..7
+    const uint64_t pol_a = policy_evict_last(); // gathered rows are re-read by every N tile
+    const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
+    const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
+    int64_t it = 0;  // K blocks issued by this thread across all of its tiles
     bool alive = true;
     for (int t = blockIdx.x; t < num_tiles && alive; t += gridDim.x) {
       const TileCoord tc = tile_coord(t, p);
-      // Index staging: lane l owns rows 4l..4l+3 of the tile. Rows past the chunk reuse the
-      // chunk's first row (valid memory; the store clips them).
-      int32_t rows4[4];
+      // Index staging: resolve this thread's 8 rows once per tile. Rows past the chunk and
+      // rows with a bad index are zero-filled (src size 0: no global read).
+      const char* src[8];
+      uint32_t valid = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = tc.m * BM + lane * 4 + q;
-        bool ok = true;
-        rows4[q] = (r < p.rows) ? resolve_row(p, p.row_begin + r, ok) : 0;
+      for (int j = 0; j < 8; ++j) {
+        const int r = tc.m * BM + row0 + 16 * j;
+        bool ok = false;
+        int32_t row = 0;
+        if (r < p.rows) row = resolve_row(p, p.row_begin + r, ok);
+        src[j] = hbase + static_cast<int64_t>(row) * row_bytes;
+        valid |= (ok ? 1u : 0u) << j;
       }
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        int ok_w = 1;
-        if (lane == 0) ok_w = wait_phase(sm.empty(stage), phase ^ 1u, sm, p) ? 1 : 0;
-        ok_w = __shfl_sync(0xffffffffu, ok_w, 0);
-        if (!ok_w) { alive = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(sm.full(stage), A_STAGE + B_STAGE);
-          tma_load_2d(sm.b(stage), &tm_w, kb * BK, tc.n * BN, sm.full(stage), pol_w);
+        // Publish the K block issued A_LAG iterations ago: its copies are complete, make them
+        // visible to the tensor cores' (async-proxy) reads, then arrive on its full barrier.
+        if (it >= A_LAG) {
+          cp_async_wait<A_LAG - 1>();
+          fence_proxy_async_smem();
+          mbar_arrive(sm.full(static_cast<int>((it - A_LAG) % STAGES)));
         }
-        __syncwarp();
-        tma_gather4(sm.a(stage) + lane * 4 * 128, &tm_h, kb * BK, rows4[0], rows4[1], rows4[2],
-                    rows4[3], sm.full(stage), pol_a);
-        ++issued;
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        const int stage = static_cast<int>(it % STAGES);
+        const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
+        if (!wait_phase(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
+        const bool k_in = kb * BK + chunk * 8 < p.d;  // d % 8 == 0: pieces are all in or out
+        const uint32_t a_stage = sm.a(stage);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = row0 + 16 * j;
+          const uint32_t dst = a_stage + r * 128 + ((chunk ^ (r & 7)) << 4);
+          const bool live = k_in && ((valid >> j) & 1u);
+          // a zero-filling copy still names an address: keep it at the start of H
+          cp_async_16(dst, live ? src[j] + static_cast<int64_t>(kb) * (BK * 2) : hbase,
+                      live ? 16u : 0u, pol_a);
+        }
+        cp_async_commit();
+        ++it;
       }
     }
-    if (!alive && lane == 0) {
-      // Let every load already issued land before the CTA can exit.
-      for (int s = 0; s < STAGES; ++s) {
-        // last K block issued on stage s
-        const int64_t last = issued - 1 - ((issued - 1 - s) % STAGES + STAGES) % STAGES;
-        if (issued > 0 && last >= 0) drain_wait(sm.full(s), static_cast<uint32_t>((last / STAGES) & 1));
-      }
+    cp_async_wait<0>();
+    if (alive) {
+      fence_proxy_async_smem();
+      for (int64_t q = (it > A_LAG ? it - A_LAG : 0); q < it; ++q)
+        mbar_arrive(sm.full(static_cast<int>(q % STAGES)));
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -381,13 +430,13 @@ cudaError_t gather_gemm_prepare(bool out_f32) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
-cudaError_t gather_gemm_launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                               const CUtensorMap& tm_out, const GatherGemmParams& p,
-                               bool out_f32, int grid, cudaStream_t stream) {
+cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
+                               const GatherGemmParams& p, bool out_f32, int grid,
+                               cudaStream_t stream) {
   if (out_f32)
-    gather_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, tm_out, p);
+    gather_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_w, tm_out, p);
   else
-    gather_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, tm_out, p);
+    gather_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_w, tm_out, p);
   return cudaGetLastError();
 }
 

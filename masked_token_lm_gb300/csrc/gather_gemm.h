@@ -12,6 +12,7 @@ constexpr uint32_t MOSAIC_STATUS_INDEX = 1u;    // a mask index / CSR offset was
 constexpr uint32_t MOSAIC_STATUS_TIMEOUT = 2u;  // a bounded wait gave up
 
 struct GatherGemmParams {
+  const void* hidden;           // bf16 [L_tot, d]
   const int32_t* idx;           // [M_total] mask indices (whole list, not just this chunk)
   const int32_t* seq_offsets;   // CSR [B+1] or nullptr
   const int32_t* mask_offsets;  // CSR [B+1] or nullptr
@@ -22,6 +23,7 @@ struct GatherGemmParams {
   int32_t rows;                 // positions in this chunk
   int32_t chunk_index;
   int32_t V;
+  int32_t d;
   int32_t k_blocks;             // ceil(d / BK)
   int32_t m_tiles, n_tiles;     // ceil(rows / BM), ceil(V / BN)
   int32_t group_m;              // M tiles per raster group
@@ -35,8 +37,8 @@ int gather_gemm_block_n();
 int gather_gemm_block_k();
 int gather_gemm_epi_cols(bool out_f32);
 cudaError_t gather_gemm_prepare(bool out_f32);
-cudaError_t gather_gemm_launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                               const CUtensorMap& tm_out, const GatherGemmParams& p,
-                               bool out_f32, int grid, cudaStream_t stream);
+cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
+                               const GatherGemmParams& p, bool out_f32, int grid,
+                               cudaStream_t stream);
 
 }  // namespace mosaic

@@ -1,4 +1,4 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA (tiled, gather4, store) and the
+// Inline-PTX building blocks for sm_103a: mbarriers, TMA (tiled load, store), cp.async and the
 // tcgen05 tensor-core / tensor-memory instructions. Each wrapper is one instruction (or a
 // bounded loop around one) so that the kernels read like the hardware pipeline they drive.
 #pragma once
@@ -65,18 +65,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Row gather: four rows y0..y3 (each one box of width x..x+box) land back to back at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3,
-                                            uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
-      "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x,
                                              int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
@@ -98,6 +86,25 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // Wait until all committed store groups are complete (writes visible).
 __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// 16-byte global->shared copy through L2 (bypassing L1). src_bytes = 0 zero-fills the
+// destination without reading global memory.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes,
+                                            uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed cp.async groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
