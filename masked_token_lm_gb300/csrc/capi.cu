@@ -23,6 +23,7 @@
 struct mosaic_handle {
   int device = 0;
   int num_sms = 0;
+  int max_clusters[2][2] = {};  // [out_f32][pair]: clusters resident at once
   uint32_t* d_status = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int64_t launches = 0;
@@ -89,13 +90,13 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* b
   return r == CUDA_SUCCESS;
 }
 
-// M tiles per raster group: as many as keep the group's gathered rows (BM x d bf16 each)
-// within ~48 MiB of L2, so that W panels are streamed once per group.
-int pick_group_m(int m_tiles, int64_t d) {
-  const int64_t per_tile = static_cast<int64_t>(mosaic::gather_gemm_block_m()) * d * 2;
-  int64_t g = (48ll << 20) / per_tile;
+// M units per raster group: as many as keep the group's gathered rows (cluster_m x BM x d
+// bf16 per unit) within ~48 MiB of L2, so that W panels are streamed once per group.
+int pick_group_u(int m_units, int cm, int64_t d) {
+  const int64_t per_unit = static_cast<int64_t>(cm) * mosaic::gather_gemm_block_m() * d * 2;
+  int64_t g = (48ll << 20) / per_unit;
   if (g < 1) g = 1;
-  if (g > m_tiles) g = m_tiles;
+  if (g > m_units) g = m_units;
   return static_cast<int>(g);
 }
 
@@ -117,13 +118,19 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
     return fail(MOSAIC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
                 device, prop.major, prop.minor);
   if (!encode_fn()) return fail(MOSAIC_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
-  for (bool f32 : {false, true}) {
-    e = mosaic::gather_gemm_prepare(f32);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  }
   auto* h = new mosaic_handle();
   h->device = device;
   h->num_sms = prop.multiProcessorCount;
+  for (int f32 = 0; f32 < 2; ++f32) {
+    for (int pair = 0; pair < 2 && e == cudaSuccess; ++pair) {
+      e = mosaic::gather_gemm_prepare(f32 != 0, pair != 0, &h->max_clusters[f32][pair]);
+      if (e == cudaSuccess && h->max_clusters[f32][pair] < 1) e = cudaErrorInvalidConfiguration;
+    }
+    if (e != cudaSuccess) {
+      delete h;
+      return cuda_fail(e, "kernel attributes / cluster occupancy");
+    }
+  }
   e = cudaMalloc(&h->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 256);
   if (e != cudaSuccess) {
@@ -213,8 +220,13 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
   const int64_t m_tiles_max = (cr + BM - 1) / BM;
   if (m_tiles_max * n_tiles >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "too many tiles");
 
+  // A CTA pair (256-row tiles) whenever there is more than one M tile; the choice is fixed for
+  // the whole call (from the largest chunk) so every chunk runs the same kernel.
+  const bool pair = m_tiles_max >= 2;
+  const int cm = pair ? 2 : 1;
   CUtensorMap tm_w, tm_out;
-  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d, BN, BK))
+  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d,
+                 mosaic::gather_gemm_w_box_rows(pair), BK))
     return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -241,11 +253,14 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     p.k_blocks = static_cast<int32_t>((d + BK - 1) / BK);
     p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
     p.n_tiles = static_cast<int32_t>(n_tiles);
-    p.group_m = pick_group_m(p.m_tiles, d);
+    p.cluster_m = cm;
+    p.m_units = (p.m_tiles + cm - 1) / cm;
+    p.group_u = pick_group_u(p.m_units, cm, d);
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
+    const int64_t clusters = h->max_clusters[f32 ? 1 : 0][pair ? 1 : 0];
+    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
     e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     ++h->launches;

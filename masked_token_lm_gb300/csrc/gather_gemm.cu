@@ -7,29 +7,40 @@
 // the hidden states of all tokens through the mask indices (indirect addressing), tiles the
 // GEMM over the GPU's compute units and keeps the gathered rows on chip, so no gathered [M, d]
 // buffer is ever written. The pages' kernel targeted RTX 3090 / A100; this one is designed for
-// Blackwell instead:
+// Blackwell instead.
 //
+// Roles (per CTA, 320 threads):
 //   warps 6..9  A gather: each of the 128 threads resolves 8 of the tile's mask indices to
 //               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
 //               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
 //               a STAGES-deep shared-memory ring (8 threads cover one 128-byte row segment).
-//   warp 0      W stream: one thread issues a 2-D TMA load of the 256 x 64 W tile per K block.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16) into a
-//               double-buffered TMEM accumulator (2 x 256 columns) and commits stage releases.
+//   warp 0      W stream: one thread issues a 2-D TMA load of the W tile per K block.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
+//               accumulator (2 x 256 fp32 columns) and commits stage releases.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator, round to bf16 (or keep fp32), write
 //               128-byte-swizzled staging tiles and TMA-store them; rows past the chunk are
 //               clipped by the store's tensor map.
+//
+// PAIR = true (the normal case): two CTAs of a cluster form a pair that computes a 256 x 256
+// tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), issued by the leader CTA.
+// Each CTA gathers its own 128 A rows and loads its own 128-row half of the W tile, so every
+// SM takes in 32 KiB per K block instead of 48 KiB; per-SM ingress was the measured limit of
+// the single-CTA 128 x 256 form. The leader's stage barriers collect the whole pair: its W
+// expect_tx covers both halves (each CTA's cta_group::2 TMA load reports its bytes there), and
+// an otherwise idle thread of the peer relays the peer's gather completions with one
+// cluster-scope arrive per K block. Commits multicast to both CTAs. PAIR = false runs
+// 128 x 256 tiles on one CTA (problems with a single M tile).
 //
 // The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
 // 32 gather4 instructions a 128-row K block needs held the kernel to ~26 % of the tensor peak,
 // while the same bytes through the load/store units keep the tensor pipe fed.
 //
-// Tiles are walked by a static persistent schedule: within a group of M tiles, N panels outer
-// and M tiles inner, so each W panel is fetched from HBM once per group while the gathered A
-// rows of the group stay in L2.
+// Tiles are walked by a static persistent schedule over units (one M tile per CTA of the pair,
+// one N panel): within a group of M units, N panels outer and M units inner, so each W panel is
+// fetched from HBM once per group while the gathered A rows of the group stay in L2.
 //
 // Every wait is bounded (globaltimer); a wait that runs out records MOSAIC status bit 2, makes
-// all roles stop, drains in-flight copies and MMAs, frees TMEM and returns.
+// all roles stop, lets in-flight copies and MMAs finish, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -42,71 +53,90 @@ namespace mosaic {
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;  // 64 bf16 = 128 B = one swizzle row
+constexpr int BM = 128;  // rows of D per CTA
+constexpr int BN = 256;  // columns of D per tile
+constexpr int BK = 64;   // 64 bf16 = 128 B = one swizzle row
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
-constexpr int B_STAGE = BN * BK * 2;  // 32 KiB
 constexpr int EPI_BUF = BM * 128;     // 128 rows x 128 B
 constexpr int EPI_BUFS = 2;
 constexpr int TMEM_COLS = 2 * BN;     // two accumulators
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
 constexpr int A_WARP0 = 6;
-constexpr int A_THREADS = 128;
+constexpr int A_WARPS = 4;
+constexpr int A_THREADS = 32 * A_WARPS;
 constexpr int NUM_THREADS = (A_WARP0 * 32) + A_THREADS;  // 320
-constexpr int A_LAG = STAGES - 1;  // K blocks a gather thread keeps in flight before publishing
 
-constexpr int SMEM_A_OFF = 0;
-constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE;
-constexpr int SMEM_EPI_OFF = SMEM_B_OFF + STAGES * B_STAGE;
-constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_BUFS * EPI_BUF;
-// barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_MISC_OFF = SMEM_BAR_OFF + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC_OFF + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-B alignment of the base
+template <bool PAIR>
+struct Cfg {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // W rows per CTA per tile
+  static constexpr int B_STAGE = B_ROWS * BK * 2;    // 16 or 32 KiB
+  // K blocks a gather warp keeps in flight before publishing one: half the ring, so copies
+  // get STAGES/2 K blocks to land and the MMA keeps STAGES/2 - 1 published blocks queued.
+  static constexpr int A_LAG = STAGES / 2;
+  static constexpr int SMEM_A_OFF = 0;
+  static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE;
+  static constexpr int SMEM_EPI_OFF = SMEM_B_OFF + STAGES * B_STAGE;
+  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_BUFS * EPI_BUF;
+  // full, empty, afull (peer gather -> relay), tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  static constexpr int SMEM_MISC_OFF = (SMEM_BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
+  // misc: tmem slot, abort flag, epilogue verdict, pad; 16-byte relay signal slot
+  static constexpr int SMEM_BYTES = SMEM_MISC_OFF + 32 + 1024;  // + 1024-B alignment slack
+  // Arrivals per phase on the (leader's) full barrier: its expect_tx and one per local gather
+  // warp. The bytes it expects: W of both CTAs and, for a pair, the 16-byte signal with which
+  // the peer reports that its gathered rows have landed. On the (leader's) tempty barrier: one
+  // arrive per CTA.
+  static constexpr int FULL_COUNT = 1 + A_WARPS;
+  static constexpr int TEMPTY_COUNT = PAIR ? 2 : 1;
+  static constexpr int SIGNAL_BYTES = 16;
+  static constexpr uint32_t W_TX = (PAIR ? 2 : 1) * B_STAGE + (PAIR ? SIGNAL_BYTES : 0);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-
+template <bool PAIR>
 struct Smem {
+  using C = Cfg<PAIR>;
   uint8_t* base;
-  __device__ uint32_t a(int s) const { return smem_u32(base + SMEM_A_OFF + s * A_STAGE); }
-  __device__ uint32_t b(int s) const { return smem_u32(base + SMEM_B_OFF + s * B_STAGE); }
-  __device__ uint32_t epi(int j) const { return smem_u32(base + SMEM_EPI_OFF + j * EPI_BUF); }
-  __device__ uint32_t full(int s) const { return smem_u32(base + SMEM_BAR_OFF + s * 8); }
-  __device__ uint32_t empty(int s) const {
-    return smem_u32(base + SMEM_BAR_OFF + (STAGES + s) * 8);
+  __device__ uint32_t a(int s) const { return smem_u32(base + C::SMEM_A_OFF + s * A_STAGE); }
+  __device__ uint32_t b(int s) const { return smem_u32(base + C::SMEM_B_OFF + s * C::B_STAGE); }
+  __device__ uint32_t epi(int j) const { return smem_u32(base + C::SMEM_EPI_OFF + j * EPI_BUF); }
+  __device__ uint32_t bar(int i) const { return smem_u32(base + C::SMEM_BAR_OFF + i * 8); }
+  __device__ uint32_t full(int s) const { return bar(s); }
+  __device__ uint32_t empty(int s) const { return bar(C::STAGES + s); }
+  __device__ uint32_t afull(int s) const { return bar(2 * C::STAGES + s); }
+  __device__ uint32_t tfull(int j) const { return bar(3 * C::STAGES + j); }
+  __device__ uint32_t tempty(int j) const { return bar(3 * C::STAGES + 2 + j); }
+  __device__ uint32_t drain() const { return bar(3 * C::STAGES + 4); }
+  __device__ uint32_t* tmem_slot() const {
+    return reinterpret_cast<uint32_t*>(base + C::SMEM_MISC_OFF);
   }
-  __device__ uint32_t tfull(int j) const {
-    return smem_u32(base + SMEM_BAR_OFF + (2 * STAGES + j) * 8);
-  }
-  __device__ uint32_t tempty(int j) const {
-    return smem_u32(base + SMEM_BAR_OFF + (2 * STAGES + 2 + j) * 8);
-  }
-  __device__ uint32_t drain() const { return smem_u32(base + SMEM_BAR_OFF + (2 * STAGES + 4) * 8); }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + SMEM_MISC_OFF); }
   __device__ volatile int* abort_flag() const {
-    return reinterpret_cast<volatile int*>(base + SMEM_MISC_OFF + 4);
+    return reinterpret_cast<volatile int*>(base + C::SMEM_MISC_OFF + 4);
   }
   __device__ volatile int* epi_go() const {
-    return reinterpret_cast<volatile int*>(base + SMEM_MISC_OFF + 8);
+    return reinterpret_cast<volatile int*>(base + C::SMEM_MISC_OFF + 8);
   }
+  __device__ uint32_t signal_slot() const { return smem_u32(base + C::SMEM_MISC_OFF + 16); }
 };
 
 // Bounded wait on an mbarrier phase. Returns false (after recording the timeout) if the wait
-// ran out or another role already gave up.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Smem& sm,
+// ran out or another role of this CTA already gave up. CLUSTER: acquire at cluster scope, for
+// barriers the peer CTA arrives on with data to hand over.
+template <bool CLUSTER, bool PAIR>
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Smem<PAIR>& sm,
                                            const GatherGemmParams& p) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((++n & 63u) == 0) {
       if (*sm.abort_flag()) return false;
       if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -118,7 +148,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   }
 }
 
-// Wait used while shutting down after an abort: fixed limit, no status side effects.
+// Wait used while shutting down: fixed limit, no status side effects.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -128,7 +158,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // Hidden row of flat mask position i (0 <= i < M). Sets ok = false for an index outside its
 // sequence or outside H; the returned row is then 0 (a safe address) and the output row is
-// zero-filled by the epilogue.
+// zero-filled.
 __device__ __forceinline__ int32_t resolve_row(const GatherGemmParams& p, int32_t i, bool& ok) {
   const int32_t v = __ldg(p.idx + i);
   if (p.mask_offsets == nullptr) {
@@ -152,39 +182,49 @@ struct TileCoord {
   int m, n;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, const GatherGemmParams& p) {
-  const int group_tiles = p.group_m * p.n_tiles;
-  const int g = t / group_tiles;
-  const int rem = t - g * group_tiles;
-  const int m_first = g * p.group_m;
-  const int gm = min(p.group_m, p.m_tiles - m_first);
+// Work unit u = (cluster_m consecutive M tiles, one N panel). Units are rastered in groups of
+// group_u M units: N panels outer, M units inner. CTA `rank` of the pair takes M tile
+// mu * cluster_m + rank of the unit.
+__device__ __forceinline__ TileCoord unit_coord(int u, int rank, const GatherGemmParams& p) {
+  const int group_units = p.group_u * p.n_tiles;
+  const int g = u / group_units;
+  const int rem = u - g * group_units;
+  const int mu_first = g * p.group_u;
+  const int gm = min(p.group_u, p.m_units - mu_first);
   TileCoord c;
   c.n = rem / gm;
-  c.m = m_first + (rem - c.n * gm);
+  c.m = (mu_first + (rem - c.n * gm)) * p.cluster_m + rank;
   return c;
 }
 
-template <bool OUT_F32>
+template <bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_out,
                        const GatherGemmParams p) {
+  using C = Cfg<PAIR>;
+  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  Smem sm;
+  Smem<PAIR> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit0 = static_cast<int>(blockIdx.x) / p.cluster_m;
+  const int unit_stride = static_cast<int>(gridDim.x) / p.cluster_m;
+  const int num_units = p.m_units * p.n_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(sm.full(s), 1 + A_THREADS);  // W arrive.expect_tx + every gather thread
-      mbar_init(sm.empty(s), 1);  // MMA commit
+      mbar_init(sm.full(s), C::FULL_COUNT);  // used in the leader (or the single CTA)
+      mbar_init(sm.empty(s), 1);             // MMA commit (multicast to both CTAs of a pair)
+      mbar_init(sm.afull(s), A_WARPS);       // peer of a pair: its gather warps, for the relay
     }
     for (int j = 0; j < 2; ++j) {
-      mbar_init(sm.tfull(j), 1);             // MMA commit
-      mbar_init(sm.tempty(j), EPI_THREADS);  // every epilogue thread
+      mbar_init(sm.tfull(j), 1);                 // MMA commit
+      mbar_init(sm.tempty(j), C::TEMPTY_COUNT);  // epilogue (of both CTAs of a pair)
     }
     mbar_init(sm.drain(), 1);
     *sm.abort_flag() = 0;
@@ -199,11 +239,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_out);
   }
-  if (warp == 1) tmem_alloc<TMEM_COLS>(smem_u32(sm.tmem_slot()));
+  if (warp == 1) tmem_alloc<TMEM_COLS, PAIR>(smem_u32(sm.tmem_slot()));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The peer arrives on this CTA's barriers: wait until both CTAs have initialised theirs.
+  if (PAIR) cluster_sync();
   const uint32_t tmem_base = *sm.tmem_slot();
+  // Barriers that both CTAs of a pair report to live in the leader.
+  auto full_c = [&](int s) { return PAIR ? mapa_shared(sm.full(s), 0) : sm.full(s); };
+  auto tempty_c = [&](int j) { return PAIR ? mapa_shared(sm.tempty(j), 0) : sm.tempty(j); };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- W stream (TMA)
@@ -211,25 +256,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t pol_w = policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
-      int64_t issued = 0;  // K blocks issued (for the drain after an abort)
-      bool alive = true;
-      for (int t = blockIdx.x; t < num_tiles && alive; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p);
+      for (int u = unit0; u < num_units; u += unit_stride) {
+        const TileCoord tc = unit_coord(u, rank, p);
+        bool alive = true;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
-          mbar_arrive_expect_tx(sm.full(stage), B_STAGE);
-          tma_load_2d(sm.b(stage), &tm_w, kb * BK, tc.n * BN, sm.full(stage), pol_w);
-          ++issued;
+          if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
+          const int y = tc.n * BN + rank * C::B_ROWS;  // this CTA's half of the W tile
+          if constexpr (PAIR) {
+            // The leader expects both halves; each CTA's load lands in its own shared memory
+            // and reports its bytes to the leader's barrier.
+            if (leader) mbar_arrive_expect_tx(sm.full(stage), C::W_TX);
+            tma_load_2d_pair(sm.b(stage), &tm_w, kb * BK, y, full_c(stage), pol_w);
+          } else {
+            mbar_arrive_expect_tx(sm.full(stage), C::W_TX);
+            tma_load_2d(sm.b(stage), &tm_w, kb * BK, y, sm.full(stage), pol_w);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-      }
-      if (!alive) {
-        // Let every W load already issued land before the CTA can exit.
-        for (int s = 0; s < STAGES; ++s) {
-          const int64_t last = issued - 1 - ((issued - 1 - s) % STAGES + STAGES) % STAGES;
-          if (issued > 0 && last >= 0)
-            drain_wait(sm.full(s), static_cast<uint32_t>((last / STAGES) & 1));
-        }
+        if (!alive) break;
       }
     }
     __syncwarp();
@@ -241,10 +285,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t pol_a = policy_evict_last(); // gathered rows are re-read by every N tile
     const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
     const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
-    int64_t it = 0;  // K blocks issued by this thread across all of its tiles
+    int64_t it = 0;  // K blocks issued by this warp across all of its tiles
     bool alive = true;
-    for (int t = blockIdx.x; t < num_tiles && alive; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, p);
+    for (int u = unit0; u < num_units && alive; u += unit_stride) {
+      const TileCoord tc = unit_coord(u, rank, p);
       // Index staging: resolve this thread's 8 rows once per tile. Rows past the chunk and
       // rows with a bad index are zero-filled (src size 0: no global read).
       const char* src[8];
@@ -259,16 +303,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         valid |= (ok ? 1u : 0u) << j;
       }
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        // Publish the K block issued A_LAG iterations ago: its copies are complete, make them
-        // visible to the tensor cores' (async-proxy) reads, then arrive on its full barrier.
-        if (it >= A_LAG) {
-          cp_async_wait<A_LAG - 1>();
+        // Publish the K block issued A_LAG iterations ago: this thread's copies are complete;
+        // make them visible to the tensor cores' (async-proxy) reads, then one arrive per warp.
+        if (it >= C::A_LAG) {
+          cp_async_wait<C::A_LAG - 1>();
           fence_proxy_async_smem();
-          mbar_arrive(sm.full(static_cast<int>((it - A_LAG) % STAGES)));
+          __syncwarp();
+          if (lane == 0) {
+            const int s_old = static_cast<int>((it - C::A_LAG) % STAGES);
+            mbar_arrive(leader ? sm.full(s_old) : sm.afull(s_old));
+          }
         }
         const int stage = static_cast<int>(it % STAGES);
         const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
-        if (!wait_phase(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
+        int go = 1;
+        if (lane == 0) go = wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p) ? 1 : 0;
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) { alive = false; break; }
         const bool k_in = kb * BK + chunk * 8 < p.d;  // d % 8 == 0: pieces are all in or out
         const uint32_t a_stage = sm.a(stage);
 #pragma unroll
@@ -287,42 +338,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     cp_async_wait<0>();
     if (alive) {
       fence_proxy_async_smem();
-      for (int64_t q = (it > A_LAG ? it - A_LAG : 0); q < it; ++q)
-        mbar_arrive(sm.full(static_cast<int>(q % STAGES)));
+      __syncwarp();
+      if (lane == 0) {
+        for (int64_t q = (it > C::A_LAG ? it - C::A_LAG : 0); q < it; ++q) {
+          const int s_old = static_cast<int>(q % STAGES);
+          mbar_arrive(leader ? sm.full(s_old) : sm.afull(s_old));
+        }
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (PAIR && !leader && lane == 0) {
+      // Relay (peer CTA of a pair): once this CTA's gather warps have published a stage (their
+      // copies landed and were fenced to the async proxy), report it to the leader's full
+      // barrier through the async proxy: a 16-byte shared-to-shared bulk copy whose complete_tx
+      // lands there. A cluster-scope release arrive instead was measured to cost ~0.8 us per
+      // K block, which capped the pair at ~30 % of the tensor peak.
+      const uint32_t dst = mapa_shared(sm.signal_slot(), 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      for (int u = unit0; u < num_units && alive; u += unit_stride) {
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
+          bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool alive = true;
       bool issued_any = false;
-      for (int t = blockIdx.x; t < num_tiles && alive; t += gridDim.x) {
-        if (!wait_phase(sm.tempty(acc), acc_phase ^ 1u, sm, p)) { alive = false; break; }
+      for (int u = unit0; u < num_units && alive; u += unit_stride) {
+        if (!wait_phase<PAIR>(sm.tempty(acc), acc_phase ^ 1u, sm, p)) { alive = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase(sm.full(stage), phase, sm, p)) { alive = false; break; }
+          if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
           tc_fence_after();
           const uint64_t a0 = smem_desc_sw128(sm.a(stage));
           const uint64_t b0 = smem_desc_sw128(sm.b(stage));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
-            tc_mma_bf16(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(sm.empty(stage));  // frees the stage once these MMAs have read it
+          tc_commit<PAIR>(sm.empty(stage));  // frees the stage once these MMAs have read it
           issued_any = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!alive) break;
-        tc_commit(sm.tfull(acc));  // accumulator complete
+        tc_commit<PAIR>(sm.tfull(acc));  // accumulator complete
         if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
       }
-      if (!alive && issued_any) {
-        tc_commit(sm.drain());  // completes when every MMA issued above has finished
+      if (issued_any) {
+        // Completes when every MMA issued above (and the arrives it triggers) has finished.
+        tc_commit_local<PAIR>(sm.drain());
         drain_wait(sm.drain(), 0);
       }
     }
@@ -338,9 +413,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int buf = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, p);
-      if (et == 0) *sm.epi_go() = wait_phase(sm.tfull(acc), acc_phase, sm, p) ? 1 : 0;
+    for (int u = unit0; u < num_units; u += unit_stride) {
+      const TileCoord tc = unit_coord(u, rank, p);
+      if (et == 0) *sm.epi_go() = wait_phase<false>(sm.tfull(acc), acc_phase, sm, p) ? 1 : 0;
       named_bar_sync(1, EPI_THREADS);
       if (!*sm.epi_go()) break;
       tc_fence_after();
@@ -377,14 +452,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int j = 0; j < 32; ++j) packed[j] = 0u;
           }
         }
-        if (c == CHUNKS - 1) {
-          // All columns of this accumulator are in registers: hand it back to the MMA warp.
-          tc_fence_before();
-          mbar_arrive(sm.tempty(acc));
-        }
+        if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
         // The staging buffer is free once the store issued from it two chunks ago has read it.
         if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
         named_bar_sync(1, EPI_THREADS);
+        if (c == CHUNKS - 1 && et == 0) {
+          // All columns of this accumulator are in registers: hand it back to the MMA issuer.
+          if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
+        }
         const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
         const int sw = row_in_tile & 7;
 #pragma unroll
@@ -396,9 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
           const int x = n0 + c * COLS_PER_CHUNK;
-          if (x < p.V) {
-            tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
-          }
+          if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
           bulk_commit_group();
         }
         buf ^= 1;
@@ -410,34 +483,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  const bool aborted = *sm.abort_flag() != 0;
+  // No CTA leaves (or frees TMEM the leader's MMAs write) while its peer still works.
+  if (PAIR) cluster_sync();
+  if (aborted) {  // loads issued just before giving up: let them land before the CTA exits
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+  }
   tc_fence_after();
-  if (warp == 1) tmem_dealloc<TMEM_COLS>(tmem_base);
+  if (warp == 1) tmem_dealloc<TMEM_COLS, PAIR>(tmem_base);
+}
+
+template <bool F32, bool PAIR>
+cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<PAIR>::SMEM_BYTES;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <bool F32, bool PAIR>
+cudaError_t prepare_one(int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(gather_gemm_kernel<F32, PAIR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<PAIR>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config<F32, PAIR>((PAIR ? 2 : 1) * 64, nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR>, &cfg);
+}
+
+template <bool F32, bool PAIR>
+cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
+                       const GatherGemmParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config<F32, PAIR>(grid, stream, attr);
+  return cudaLaunchKernelEx(&cfg, gather_gemm_kernel<F32, PAIR>, tm_w, tm_out, p);
 }
 
 }  // namespace
 
-int gather_gemm_smem_bytes() { return SMEM_BYTES; }
 int gather_gemm_block_m() { return BM; }
 int gather_gemm_block_n() { return BN; }
 int gather_gemm_block_k() { return BK; }
 int gather_gemm_epi_cols(bool out_f32) { return out_f32 ? 32 : 64; }
+int gather_gemm_w_box_rows(bool pair) { return pair ? Cfg<true>::B_ROWS : Cfg<false>::B_ROWS; }
 
-cudaError_t gather_gemm_prepare(bool out_f32) {
-  if (out_f32)
-    return cudaFuncSetAttribute(gather_gemm_kernel<true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  return cudaFuncSetAttribute(gather_gemm_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters) {
+  if (out_f32) return pair ? prepare_one<true, true>(clusters) : prepare_one<true, false>(clusters);
+  return pair ? prepare_one<false, true>(clusters) : prepare_one<false, false>(clusters);
 }
 
 cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                                const GatherGemmParams& p, bool out_f32, int grid,
                                cudaStream_t stream) {
+  const bool pair = p.cluster_m == 2;
   if (out_f32)
-    gather_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_w, tm_out, p);
-  else
-    gather_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tm_w, tm_out, p);
-  return cudaGetLastError();
+    return pair ? launch_one<true, true>(tm_w, tm_out, p, grid, stream)
+                : launch_one<true, false>(tm_w, tm_out, p, grid, stream);
+  return pair ? launch_one<false, true>(tm_w, tm_out, p, grid, stream)
+              : launch_one<false, false>(tm_w, tm_out, p, grid, stream);
 }
 
 }  // namespace mosaic

@@ -26,17 +26,20 @@ struct GatherGemmParams {
   int32_t d;
   int32_t k_blocks;             // ceil(d / BK)
   int32_t m_tiles, n_tiles;     // ceil(rows / BM), ceil(V / BN)
-  int32_t group_m;              // M tiles per raster group
+  int32_t cluster_m;            // 2: a CTA pair computes 256-row tiles (cta_group::2); 1: single
+  int32_t m_units;              // ceil(m_tiles / cluster_m)
+  int32_t group_u;              // M units per raster group
   uint32_t* status;             // device status word
   uint64_t timeout_ns;          // bound on any single wait
 };
 
-int gather_gemm_smem_bytes();
 int gather_gemm_block_m();
 int gather_gemm_block_n();
 int gather_gemm_block_k();
 int gather_gemm_epi_cols(bool out_f32);
-cudaError_t gather_gemm_prepare(bool out_f32);
+int gather_gemm_w_box_rows(bool pair);
+// Sets the kernel's shared-memory attribute and reports how many clusters fit at once.
+cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters);
 cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                                const GatherGemmParams& p, bool out_f32, int grid,
                                cudaStream_t stream);
