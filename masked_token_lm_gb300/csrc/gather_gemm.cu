@@ -73,9 +73,6 @@ struct Cfg {
   static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // W rows per CTA per tile
   static constexpr int B_STAGE = B_ROWS * BK * 2;    // 16 or 32 KiB
-  // K blocks a gather warp keeps in flight before publishing one: half the ring, so copies
-  // get STAGES/2 K blocks to land and the MMA keeps STAGES/2 - 1 published blocks queued.
-  static constexpr int A_LAG = STAGES / 2;
   static constexpr int SMEM_A_OFF = 0;
   static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE;
   static constexpr int SMEM_EPI_OFF = SMEM_B_OFF + STAGES * B_STAGE;
@@ -86,10 +83,10 @@ struct Cfg {
   // misc: tmem slot, abort flag, epilogue verdict, pad; 16-byte relay signal slot
   static constexpr int SMEM_BYTES = SMEM_MISC_OFF + 32 + 1024;  // + 1024-B alignment slack
   // Arrivals per phase on the (leader's) full barrier: its expect_tx and one per local gather
-  // warp. The bytes it expects: W of both CTAs and, for a pair, the 16-byte signal with which
-  // the peer reports that its gathered rows have landed. On the (leader's) tempty barrier: one
-  // arrive per CTA.
-  static constexpr int FULL_COUNT = 1 + A_WARPS;
+  // thread (made by the hardware when that thread's copies have landed). The bytes it expects:
+  // W of both CTAs and, for a pair, the 16-byte signal with which the peer reports that its
+  // gathered rows have landed. On the (leader's) tempty barrier: one arrive per CTA.
+  static constexpr int FULL_COUNT = 1 + A_THREADS;
   static constexpr int TEMPTY_COUNT = PAIR ? 2 : 1;
   static constexpr int SIGNAL_BYTES = 16;
   static constexpr uint32_t W_TX = (PAIR ? 2 : 1) * B_STAGE + (PAIR ? SIGNAL_BYTES : 0);
@@ -220,7 +217,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(sm.full(s), C::FULL_COUNT);  // used in the leader (or the single CTA)
       mbar_init(sm.empty(s), 1);             // MMA commit (multicast to both CTAs of a pair)
-      mbar_init(sm.afull(s), A_WARPS);       // peer of a pair: its gather warps, for the relay
+      mbar_init(sm.afull(s), A_THREADS);     // peer of a pair: its gather threads, for the relay
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(sm.tfull(j), 1);                 // MMA commit
@@ -303,17 +300,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         valid |= (ok ? 1u : 0u) << j;
       }
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        // Publish the K block issued A_LAG iterations ago: this thread's copies are complete;
-        // make them visible to the tensor cores' (async-proxy) reads, then one arrive per warp.
-        if (it >= C::A_LAG) {
-          cp_async_wait<C::A_LAG - 1>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int s_old = static_cast<int>((it - C::A_LAG) % STAGES);
-            mbar_arrive(leader ? sm.full(s_old) : sm.afull(s_old));
-          }
-        }
         const int stage = static_cast<int>(it % STAGES);
         const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
         int go = 1;
@@ -331,21 +317,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           cp_async_16(dst, live ? src[j] + static_cast<int64_t>(kb) * (BK * 2) : hbase,
                       live ? 16u : 0u, pol_a);
         }
-        cp_async_commit();
+        // Publish without waiting: the arrive happens when these copies have landed. The
+        // consumer of the stage fences them into the async proxy before the tensor cores read.
+        cp_async_arrive_noinc(leader ? sm.full(stage) : sm.afull(stage));
         ++it;
       }
     }
     cp_async_wait<0>();
-    if (alive) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        for (int64_t q = (it > C::A_LAG ? it - C::A_LAG : 0); q < it; ++q) {
-          const int s_old = static_cast<int>(q % STAGES);
-          mbar_arrive(leader ? sm.full(s_old) : sm.afull(s_old));
-        }
-      }
-    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (PAIR && !leader && lane == 0) {
@@ -361,6 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
+          fence_proxy_async_smem();  // the landed rows, for the async-proxy (MMA) reads
           bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -379,6 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
+          fence_proxy_async_smem();  // gathered rows were written by cp.async (generic proxy)
           tc_fence_after();
           const uint64_t a0 = smem_desc_sw128(sm.a(stage));
           const uint64_t b0 = smem_desc_sw128(sm.b(stage));

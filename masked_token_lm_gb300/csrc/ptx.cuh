@@ -154,6 +154,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                : "memory");
 }
 
+// Arrive on `bar` (without raising its expected count) once every cp.async this thread has
+// issued so far has completed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
