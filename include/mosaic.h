@@ -136,6 +136,47 @@ MOSAIC_API int64_t mosaic_launch_count(const mosaic_handle* handle);
 /* Text of the last error produced on the calling thread ("" if none). */
 MOSAIC_API const char* mosaic_last_error_string(void);
 
+/*
+ * Allocation-free variant of mosaic_masked_logits (no counterpart in the Mosaic pages; it
+ * exists for callers that cannot allocate device memory).
+ *
+ * Who needs it: code whose device memory is owned entirely by someone else -- a global
+ * memory planner or arena that reserves and binds the whole workspace up front, a serving
+ * loop where a cudaMalloc would synchronise the device, or a host that only hands this
+ * library its input and output buffers. mosaic_create() allocates a status word, so such a
+ * caller cannot hold a handle; this entry point needs none and allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *
+ * Arguments, layouts and semantics are those of mosaic_masked_logits (same kernel, same
+ * results bit for bit), on the CURRENT CUDA device. Instead of the handle's status word it
+ * uses a status word per chunk held in a fixed device array inside the library, of
+ * MOSAIC_NOALLOC_MAX_CHUNKS words; a call that needs more chunks than that (ceil(M /
+ * chunk_rows), 1 when chunking is off) is rejected with MOSAIC_ERR_UNSUPPORTED before
+ * anything is enqueued. Every GPU that loads the library holds that array until exit.
+ *
+ * chunk_status   optional HOST array of at least that many uint32 words. NULL: the call is
+ *                asynchronous and reports only argument errors. Non-NULL: the call waits for
+ *                `stream`, copies each chunk's status word there (bit 1: a bad mask index or
+ *                CSR offsets, bit 2: a bounded wait ran out) and returns MOSAIC_ERR_INDEX /
+ *                MOSAIC_ERR_TIMEOUT / MOSAIC_OK accordingly.
+ *
+ * The first call on a device sets that device up (kernel attributes, occupancy, the array's
+ * device address); make it before any CUDA stream capture. All calls share the one array,
+ * which keeps the last call's words: each call clears the words it uses on `stream` before
+ * its kernels run, so calls that overlap on the GPU (different streams, no ordering) race
+ * on the status words and their reported status is unreliable; the logits are unaffected.
+ */
+#define MOSAIC_NOALLOC_MAX_CHUNKS 4096
+MOSAIC_API mosaic_status mosaic_masked_logits_noalloc(const void* hidden, int64_t L_tot,
+                                                      int64_t d, const int32_t* mask_idx,
+                                                      int64_t M, const int32_t* seq_offsets,
+                                                      const int32_t* mask_offsets, int32_t B,
+                                                      const void* W, int64_t V, void* out,
+                                                      mosaic_dtype out_dtype,
+                                                      int64_t chunk_rows, mosaic_chunk_cb cb,
+                                                      void* user, uint32_t* chunk_status,
+                                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -269,4 +269,169 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
   return MOSAIC_OK;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free entry point. Its scratch (one status word per chunk) lives in this fixed
+// device array instead of memory from cudaMalloc; host code must not use the array's name as a
+// device address, so each device's address is looked up once with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------------------------
+
+static __device__ __align__(256) uint32_t g_noalloc_status[MOSAIC_NOALLOC_MAX_CHUNKS];
+
+namespace {
+
+struct NoallocDevice {
+  bool ready = false;
+  int num_sms = 0;
+  int max_clusters[2][2] = {};
+  uint32_t* status = nullptr;  // device address of g_noalloc_status on this device
+};
+
+constexpr int kMaxDevices = 64;
+NoallocDevice g_noalloc_dev[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: kernel attributes, occupancy, array address.
+mosaic_status noalloc_setup(int device, NoallocDevice** out) {
+  if (device < 0 || device >= kMaxDevices) return fail(MOSAIC_ERR_UNSUPPORTED, "device id %d", device);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoallocDevice& nd = g_noalloc_dev[device];
+  if (!nd.ready) {
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(MOSAIC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  device, prop.major, prop.minor);
+    if (!encode_fn()) return fail(MOSAIC_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    for (int f32 = 0; f32 < 2; ++f32)
+      for (int pair = 0; pair < 2; ++pair) {
+        e = mosaic::gather_gemm_prepare(f32 != 0, pair != 0, &nd.max_clusters[f32][pair]);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel attributes / cluster occupancy");
+        if (nd.max_clusters[f32][pair] < 1) return fail(MOSAIC_ERR_CUDA, "kernel cannot be resident");
+      }
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the status array");
+    nd.status = static_cast<uint32_t*>(ptr);
+    nd.num_sms = prop.multiProcessorCount;
+    nd.ready = true;
+  }
+  *out = &nd;
+  return MOSAIC_OK;
+}
+
+}  // namespace
+
+mosaic_status mosaic_masked_logits_noalloc(const void* hidden, int64_t L_tot, int64_t d,
+                                           const int32_t* mask_idx, int64_t M,
+                                           const int32_t* seq_offsets,
+                                           const int32_t* mask_offsets, int32_t B,
+                                           const void* W, int64_t V, void* out,
+                                           mosaic_dtype out_dtype, int64_t chunk_rows,
+                                           mosaic_chunk_cb cb, void* user,
+                                           uint32_t* chunk_status, void* stream_ptr) {
+  if (M < 0) return fail(MOSAIC_ERR_INVALID_ARG, "M < 0");
+  if (M >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "M >= 2^31");
+  if (out_dtype != MOSAIC_BF16 && out_dtype != MOSAIC_F32)
+    return fail(MOSAIC_ERR_INVALID_ARG, "unknown out_dtype %d", static_cast<int>(out_dtype));
+  if ((seq_offsets == nullptr) != (mask_offsets == nullptr))
+    return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs both seq_offsets and mask_offsets");
+  const bool csr = seq_offsets != nullptr;
+  if (csr && B < 1) return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs B >= 1");
+  const bool chunked = chunk_rows > 0 && chunk_rows < M;
+  if (chunked && !cb) return fail(MOSAIC_ERR_INVALID_ARG, "chunking on (chunk_rows < M) needs a callback");
+  if (M == 0) return MOSAIC_OK;
+  if (!hidden || !W || !out || !mask_idx)
+    return fail(MOSAIC_ERR_INVALID_ARG, "NULL hidden, W, out or mask_idx");
+  if (d < 1 || V < 1 || L_tot < 1) return fail(MOSAIC_ERR_INVALID_ARG, "d, V and L_tot must be >= 1");
+  if (d % 8 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 8 (16-byte rows)");
+  if (V % 8 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "V must be a multiple of 8 (16-byte rows)");
+  if (L_tot >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "L_tot >= 2^31");
+  if (V >= (1ll << 31) || d >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "V or d too large");
+  if (!aligned16(hidden) || !aligned16(W) || !aligned16(out))
+    return fail(MOSAIC_ERR_INVALID_ARG, "hidden, W and out must be 16-byte aligned");
+  const int64_t cr = chunked ? chunk_rows : M;
+  const int64_t n_chunks = (M + cr - 1) / cr;
+  if (n_chunks > MOSAIC_NOALLOC_MAX_CHUNKS)
+    return fail(MOSAIC_ERR_UNSUPPORTED,
+                "%lld chunks exceed the %d status words of the allocation-free entry point; "
+                "raise chunk_rows or use mosaic_masked_logits",
+                static_cast<long long>(n_chunks), MOSAIC_NOALLOC_MAX_CHUNKS);
+
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  NoallocDevice* nd = nullptr;
+  mosaic_status st = noalloc_setup(device, &nd);
+  if (st != MOSAIC_OK) return st;
+  if (!is_device_ptr(hidden, device) || !is_device_ptr(W, device) ||
+      !is_device_ptr(out, device) || !is_device_ptr(mask_idx, device) ||
+      (csr && (!is_device_ptr(seq_offsets, device) || !is_device_ptr(mask_offsets, device))))
+    return fail(MOSAIC_ERR_INVALID_ARG, "every array must be device memory of device %d", device);
+
+  const bool f32 = out_dtype == MOSAIC_F32;
+  const int BM = mosaic::gather_gemm_block_m(), BN = mosaic::gather_gemm_block_n(),
+            BK = mosaic::gather_gemm_block_k();
+  const int64_t n_tiles = (V + BN - 1) / BN;
+  const int64_t m_tiles_max = (cr + BM - 1) / BM;
+  if (m_tiles_max * n_tiles >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "too many tiles");
+  const bool pair = m_tiles_max >= 2;
+  const int cm = pair ? 2 : 1;
+  CUtensorMap tm_w, tm_out;
+  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d,
+                 mosaic::gather_gemm_w_box_rows(pair), BK))
+    return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  // The array keeps the previous call's words: clear the ones this call uses, in stream order.
+  e = cudaMemsetAsync(nd->status, 0, static_cast<size_t>(n_chunks) * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the status words");
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t rb = c * cr;
+    const int64_t rows = (M - rb < cr) ? (M - rb) : cr;
+    const CUtensorMapDataType odt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_2d(&tm_out, odt, f32 ? 4 : 2, out, rows, V, BM, mosaic::gather_gemm_epi_cols(f32)))
+      return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for out rejected");
+    mosaic::GatherGemmParams p;
+    p.hidden = hidden;
+    p.idx = mask_idx;
+    p.seq_offsets = csr ? seq_offsets : nullptr;
+    p.mask_offsets = csr ? mask_offsets : nullptr;
+    p.L_tot = L_tot;
+    p.B = csr ? B : 0;
+    p.M_total = static_cast<int32_t>(M);
+    p.row_begin = static_cast<int32_t>(rb);
+    p.rows = static_cast<int32_t>(rows);
+    p.chunk_index = static_cast<int32_t>(c);
+    p.V = static_cast<int32_t>(V);
+    p.d = static_cast<int32_t>(d);
+    p.k_blocks = static_cast<int32_t>((d + BK - 1) / BK);
+    p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
+    p.n_tiles = static_cast<int32_t>(n_tiles);
+    p.cluster_m = cm;
+    p.m_units = (p.m_tiles + cm - 1) / cm;
+    p.group_u = pick_group_u(p.m_units, cm, d);
+    p.status = nd->status + c;  // this chunk's word of the fixed array
+    p.timeout_ns = 2000000000ull;
+    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
+    const int64_t clusters = nd->max_clusters[f32 ? 1 : 0][pair ? 1 : 0];
+    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
+    e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
+    if (cb) cb(c, rb, rows, out, user);
+  }
+  if (!chunk_status) return MOSAIC_OK;
+  e = cudaMemcpyAsync(chunk_status, nd->status, static_cast<size_t>(n_chunks) * sizeof(uint32_t),
+                      cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status words");
+  uint32_t any = 0;
+  for (int64_t c = 0; c < n_chunks; ++c) any |= chunk_status[c];
+  if (any & mosaic::MOSAIC_STATUS_TIMEOUT)
+    return fail(MOSAIC_ERR_TIMEOUT, "a bounded wait inside the kernel ran out");
+  if (any & mosaic::MOSAIC_STATUS_INDEX)
+    return fail(MOSAIC_ERR_INDEX, "a mask index (or CSR offset) was outside its sequence");
+  return MOSAIC_OK;
+}
+
 }  // extern "C"

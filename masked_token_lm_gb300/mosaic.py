@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "MOSAIC_OK", 1: "MOSAIC_ERR_INVALID_ARG", 2: "MOSAIC_ERR_UNSU
 
 MOSAIC_BF16 = 0
 MOSAIC_F32 = 1
+MOSAIC_NOALLOC_MAX_CHUNKS = 4096
 
 mosaic_chunk_cb = ctypes.CFUNCTYPE(None, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_void_p, ctypes.c_void_p)
@@ -65,6 +66,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mosaic_launch_count.restype = ctypes.c_int64
     lib.mosaic_last_error_string.argtypes = []
     lib.mosaic_last_error_string.restype = ctypes.c_char_p
+    lib.mosaic_masked_logits_noalloc.argtypes = [P, I64, I64, P, I64, P, P, I32, P, I64, P,
+                                                 ctypes.c_int, I64, mosaic_chunk_cb, P,
+                                                 ctypes.POINTER(ctypes.c_uint32), P]
+    lib.mosaic_masked_logits_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -89,6 +94,18 @@ def mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets, mas
     return load_library().mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets,
                                                mask_offsets, B, W, V, out, out_dtype, chunk_rows,
                                                cb_c, user, stream)
+
+
+def mosaic_masked_logits_noalloc(hidden, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B,
+                                 W, V, out, out_dtype, chunk_rows, cb, user, chunk_status,
+                                 stream) -> int:
+    """Raw call of the allocation-free entry point (current CUDA device, no handle).
+    chunk_status: None (asynchronous) or a ctypes uint32 array with one word per chunk."""
+    cb_c = cb if isinstance(cb, mosaic_chunk_cb) else (mosaic_chunk_cb(cb) if cb else mosaic_chunk_cb())
+    return load_library().mosaic_masked_logits_noalloc(hidden, L_tot, d, mask_idx, M, seq_offsets,
+                                                       mask_offsets, B, W, V, out, out_dtype,
+                                                       chunk_rows, cb_c, user, chunk_status,
+                                                       stream)
 
 
 def mosaic_check(handle, stream) -> int:

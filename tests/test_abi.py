@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
-        "mosaic_launch_count", "mosaic_masked_logits", "mosaic_set_wait_timeout"])
+        "mosaic_launch_count", "mosaic_masked_logits", "mosaic_masked_logits_noalloc",
+        "mosaic_set_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol(lib_path):
