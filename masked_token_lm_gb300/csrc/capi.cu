@@ -91,10 +91,10 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* b
 }
 
 // M units per raster group: as many as keep the group's gathered rows (cluster_m x BM x d
-// bf16 per unit) within ~48 MiB of L2, so that W panels are streamed once per group.
+// bf16 per unit) within ~64 MiB of L2, so that W panels are streamed once per group.
 int pick_group_u(int m_units, int cm, int64_t d) {
   const int64_t per_unit = static_cast<int64_t>(cm) * mosaic::gather_gemm_block_m() * d * 2;
-  int64_t g = (48ll << 20) / per_unit;
+  int64_t g = (64ll << 20) / per_unit;
   if (g < 1) g = 1;
   if (g > m_units) g = m_units;
   return static_cast<int>(g);
