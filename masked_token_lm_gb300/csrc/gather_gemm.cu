@@ -67,6 +67,7 @@ constexpr int A_WARP0 = 6;
 constexpr int A_WARPS = 4;
 constexpr int A_THREADS = 32 * A_WARPS;
 constexpr int NUM_THREADS = (A_WARP0 * 32) + A_THREADS;  // 320
+constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
 
 template <bool PAIR>
 struct Cfg {
@@ -81,7 +82,8 @@ struct Cfg {
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int SMEM_MISC_OFF = (SMEM_BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
   // misc: tmem slot, abort flag, epilogue verdict, pad; 16-byte relay signal slot
-  static constexpr int SMEM_BYTES = SMEM_MISC_OFF + 32 + 1024;  // + 1024-B alignment slack
+  static constexpr int SMEM_OFFS_OFF = SMEM_MISC_OFF + 32;  // seq_offsets, mask_offsets copies
+  static constexpr int SMEM_BYTES = SMEM_OFFS_OFF + 2 * OFFS_CAP * 4 + 1024;  // + alignment slack
   // Arrivals per phase on the (leader's) full barrier: its expect_tx and one per local gather
   // thread (made by the hardware when that thread's copies have landed). The bytes it expects:
   // W of both CTAs and, for a pair, the 16-byte signal with which the peer reports that its
@@ -118,6 +120,8 @@ struct Smem {
     return reinterpret_cast<volatile int*>(base + C::SMEM_MISC_OFF + 8);
   }
   __device__ uint32_t signal_slot() const { return smem_u32(base + C::SMEM_MISC_OFF + 16); }
+  __device__ int32_t* seq_offs() const { return reinterpret_cast<int32_t*>(base + C::SMEM_OFFS_OFF); }
+  __device__ int32_t* mask_offs() const { return seq_offs() + OFFS_CAP; }
 };
 
 // Bounded wait on an mbarrier phase. Returns false (after recording the timeout) if the wait
@@ -153,11 +157,18 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Hidden row of flat mask position i (0 <= i < M). Sets ok = false for an index outside its
-// sequence or outside H; the returned row is then 0 (a safe address) and the output row is
-// zero-filled.
-__device__ __forceinline__ int32_t resolve_row(const GatherGemmParams& p, int32_t i, bool& ok) {
-  const int32_t v = __ldg(p.idx + i);
+// CSR offsets as the index staging reads them: from shared memory when the batch is small
+// enough to have been staged there at kernel start, else from global memory.
+struct Offsets {
+  const int32_t* seq;   // [B+1]
+  const int32_t* mask;  // [B+1]
+};
+
+// Hidden row for flat mask position i (0 <= i < M) whose index value is v = idx[i]. Sets ok =
+// false for an index outside its sequence or outside H; the returned row is then 0 (a safe
+// address) and the output row is zero-filled.
+__device__ __forceinline__ int32_t resolve_row(const GatherGemmParams& p, const Offsets& o,
+                                               int32_t i, int32_t v, bool& ok) {
   if (p.mask_offsets == nullptr) {
     ok = (v >= 0) && (static_cast<int64_t>(v) < p.L_tot);
     return ok ? v : 0;
@@ -166,10 +177,10 @@ __device__ __forceinline__ int32_t resolve_row(const GatherGemmParams& p, int32_
   int32_t lo = 0, hi = p.B;
   while (hi - lo > 1) {
     const int32_t mid = (lo + hi) >> 1;
-    if (__ldg(p.mask_offsets + mid) <= i) lo = mid; else hi = mid;
+    if (o.mask[mid] <= i) lo = mid; else hi = mid;
   }
-  const int64_t s0 = __ldg(p.seq_offsets + lo);
-  const int64_t s1 = __ldg(p.seq_offsets + lo + 1);
+  const int64_t s0 = o.seq[lo];
+  const int64_t s1 = o.seq[lo + 1];
   const int64_t r = s0 + v;
   ok = (v >= 0) && (s0 >= 0) && (r < s1) && (s1 <= p.L_tot);
   return ok ? static_cast<int32_t>(r) : 0;
@@ -236,6 +247,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_out);
   }
+  // Index staging, part 1: small CSR batches keep their offsets in shared memory.
+  const bool offs_in_smem = p.mask_offsets != nullptr && p.B + 1 <= OFFS_CAP;
+  if (offs_in_smem) {
+    for (int i = threadIdx.x; i <= p.B; i += NUM_THREADS) {
+      sm.seq_offs()[i] = __ldg(p.seq_offsets + i);
+      sm.mask_offs()[i] = __ldg(p.mask_offsets + i);
+    }
+  }
   if (warp == 1) tmem_alloc<TMEM_COLS, PAIR>(smem_u32(sm.tmem_slot()));
   tc_fence_before();
   __syncthreads();
@@ -243,6 +262,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // The peer arrives on this CTA's barriers: wait until both CTAs have initialised theirs.
   if (PAIR) cluster_sync();
   const uint32_t tmem_base = *sm.tmem_slot();
+  const Offsets offs = offs_in_smem ? Offsets{sm.seq_offs(), sm.mask_offs()}
+                                    : Offsets{p.seq_offsets, p.mask_offsets};
   // Barriers that both CTAs of a pair report to live in the leader.
   auto full_c = [&](int s) { return PAIR ? mapa_shared(sm.full(s), 0) : sm.full(s); };
   auto tempty_c = [&](int j) { return PAIR ? mapa_shared(sm.tempty(j), 0) : sm.tempty(j); };
@@ -284,10 +305,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
     int64_t it = 0;  // K blocks issued by this warp across all of its tiles
     bool alive = true;
+    // Index staging, part 2: the mask indices of a tile are loaded one tile ahead (they land
+    // while the previous tile's K loop runs) and resolved to rows at the tile's start.
+    int32_t vnext[8];
+    auto load_idx = [&](int u, int32_t (&v)[8]) {
+      const TileCoord t = unit_coord(u, rank, p);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = t.m * BM + row0 + 16 * j;
+        v[j] = r < p.rows ? __ldg(p.idx + p.row_begin + r) : 0;
+      }
+    };
+    if (unit0 < num_units) load_idx(unit0, vnext);
     for (int u = unit0; u < num_units && alive; u += unit_stride) {
       const TileCoord tc = unit_coord(u, rank, p);
-      // Index staging: resolve this thread's 8 rows once per tile. Rows past the chunk and
-      // rows with a bad index are zero-filled (src size 0: no global read).
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = vnext[j];
+      if (u + unit_stride < num_units) load_idx(u + unit_stride, vnext);
+      // Rows past the chunk and rows with a bad index are zero-filled (src size 0: no read).
       const char* src[8];
       uint32_t valid = 0;
 #pragma unroll
@@ -295,7 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = tc.m * BM + row0 + 16 * j;
         bool ok = false;
         int32_t row = 0;
-        if (r < p.rows) row = resolve_row(p, p.row_begin + r, ok);
+        if (r < p.rows) row = resolve_row(p, offs, p.row_begin + r, v[j], ok);
         src[j] = hbase + static_cast<int64_t>(row) * row_bytes;
         valid |= (ok ? 1u : 0u) << j;
       }
@@ -402,7 +438,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int r = tc.m * BM + row_in_tile;
       bool ok = true;
       if (r < p.rows) {
-        resolve_row(p, p.row_begin + r, ok);
+        resolve_row(p, offs, p.row_begin + r, __ldg(p.idx + p.row_begin + r), ok);
         if (!ok) atomicOr(p.status, MOSAIC_STATUS_INDEX);
       }
       const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
