@@ -63,6 +63,46 @@ def algorithmic_bytes(M, V, d, out_elt):
     return 2 * V * d + 2 * M * d + out_elt * M * V + 4 * M
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per gather-GEMM launch, from an ncu
+# capture of the kernel sources with the given hash; reported only while the sources still match.
+# Entries: source hash -> {workload: bytes per launch (average over the workload's launches)}.
+MEASURED_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+    #     -k regex:gather_gemm -s 9 -c 3 python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
+    # r_m 0.1 / 0.5 / 0.9 launches: 1.136 / 1.558 / 2.153 GB
+    "986ca011272c325d": {"llada8b": 1615442603},
+}
+
+
+def kernel_source_hash():
+    """sha256 over the CUDA sources that make up the kernel and its launch."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "masked_token_lm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of a list of floats over all ranks (identity with one process)."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def rank_seed_shift(rank):
+    """Each rank draws an independent batch."""
+    return 100000 * rank
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -206,6 +246,85 @@ def bench_reference(args):
     return 0
 
 
+def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
+    """The same step end to end through the public call: every step copies its inputs (H, idx,
+    CSR offsets and W) from pinned host memory to the device and reads all logits back to pinned
+    host memory. Copies run on their own streams so that member i's read-back overlaps member
+    i+1's compute; the timed region spans all of it."""
+    import torch
+
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for c in calls:
+        hi = {"H": c["H"].cpu().pin_memory(), "idx": c["mask"].idx.cpu().pin_memory()}
+        if c is calls[0] or c["W"] is not calls[0]["W"]:
+            hi["W"] = c["W"].cpu().pin_memory()
+        for k2 in ("so", "mo"):
+            t = c["mask"].seq_offsets if k2 == "so" else c["mask"].mask_offsets
+            if t is not None:
+                hi[k2] = t.cpu().pin_memory()
+        host_in.append(hi)
+        h2d += sum(t.numel() * t.element_size() for t in hi.values())
+        ho = torch.empty((c["mask"].M, c["w"].V), dtype=c["odt"], pin_memory=True)
+        host_out.append(ho)
+        d2h += ho.numel() * ho.element_size()
+    dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items()} for hi in host_in]
+    # one device output buffer per member so read-backs can overlap the next member's compute
+    dev_out = [torch.empty_like(c["out"]) for c in calls]
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+
+    def e2e_step():
+        Wd = None
+        s_in.wait_stream(stream)  # the previous step has consumed the device input buffers
+        for c, hi, di, ho, do in zip(calls, host_in, dev_in, host_out, dev_out):
+            with torch.cuda.stream(s_in):
+                for k2, v in hi.items():
+                    di[k2].copy_(v, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            stream.wait_event(ready)
+            Wd = di.get("W", Wd)
+
+            def on_chunk(ci, rb, rows, out, ho=ho):
+                done = torch.cuda.Event()
+                done.record(stream)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    ho[rb:rb + rows].copy_(out[:rows], non_blocking=True)
+                if c["chunked"]:  # the next chunk reuses `out`: wait for its read-back
+                    drained = torch.cuda.Event()
+                    drained.record(s_out)
+                    stream.wait_event(drained)
+
+            mo.masked_logits(di["H"], di["idx"], Wd, di.get("so"), di.get("mo"), out=do,
+                             chunk_rows=c["w"].chunk_rows, on_chunk=on_chunk, stream=stream)
+        fin = torch.cuda.Event()
+        fin.record(s_out)
+        stream.wait_event(fin)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(1, min(args.steps, args.e2e_steps))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / n_e2e
+    (e_ms,) = max_over_ranks([e_ms], dev)
+    if mo.check() != mz.MOSAIC_OK:
+        raise SystemExit(f"kernel status in the e2e leg: {mz.mosaic_last_error_string()}")
+    return {"value": world * tot_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+            "steps": n_e2e, "path": "pinned host -> Mosaic.masked_logits -> pinned host"}
+
+
 def bench_cuda(args):
     import torch
 
@@ -226,7 +345,7 @@ def bench_cuda(args):
     stream = torch.cuda.current_stream()
 
     # ---- inputs resident in HBM (per-rank seeds: each rank owns an independent batch)
-    seed_shift = 100000 * rank
+    seed_shift = rank_seed_shift(rank)
     calls = []
     tot_flops = tot_bytes = 0
     for w in ws:
@@ -287,11 +406,11 @@ def bench_cuda(args):
     if st != mz.MOSAIC_OK:
         raise SystemExit(f"kernel status {st}: {mz.mosaic_last_error_string()}")
     total_ms = t_start.elapsed_time(t_end)
-    kernel_ms = sum(a.elapsed_time(b) for a, b in evs)
-    if world > 1:
-        t = torch.tensor([total_ms, kernel_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, kernel_ms = t.tolist()
+    member_ms = [0.0] * len(calls)
+    for k, (a, b) in enumerate(evs):
+        member_ms[k % len(calls)] += a.elapsed_time(b) / args.steps
+    kernel_ms = sum(member_ms) * args.steps
+    total_ms, kernel_ms, *member_ms = max_over_ranks([total_ms, kernel_ms, *member_ms], dev)
     ms_per_step = total_ms / args.steps
     value = world * tot_flops / (ms_per_step * 1e-3) / 1e12
     gbs = world * tot_bytes / (ms_per_step * 1e-3) / 1e9
@@ -299,59 +418,7 @@ def bench_cuda(args):
     # ---- end to end through the public call: pinned host inputs -> device -> logits -> host
     e2e = None
     if not args.no_e2e:
-        host_in, host_out = [], []
-        h2d = d2h = 0
-        for c in calls:
-            hi = {"H": c["H"].cpu().pin_memory(), "idx": c["mask"].idx.cpu().pin_memory()}
-            if c is calls[0] or c["W"] is not calls[0]["W"]:
-                hi["W"] = c["W"].cpu().pin_memory()
-            for k2 in ("so", "mo"):
-                t = c["mask"].seq_offsets if k2 == "so" else c["mask"].mask_offsets
-                if t is not None:
-                    hi[k2] = t.cpu().pin_memory()
-            host_in.append(hi)
-            h2d += sum(t.numel() * t.element_size() for t in hi.values())
-            full_rows = c["mask"].M
-            ho = torch.empty((full_rows, c["w"].V), dtype=c["odt"], pin_memory=True)
-            host_out.append(ho)
-            d2h += ho.numel() * ho.element_size()
-        dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items()} for hi in host_in]
-
-        def e2e_step():
-            Wd = None
-            for c, hi, di, ho in zip(calls, host_in, dev_in, host_out):
-                for k2, v in hi.items():
-                    di[k2].copy_(v, non_blocking=True)
-                Wd = di.get("W", Wd)
-
-                def on_chunk(ci, rb, rows, out, ho=ho):
-                    ho[rb:rb + rows].copy_(out[:rows], non_blocking=True)
-
-                mo.masked_logits(di["H"], di["idx"], Wd, di.get("so"), di.get("mo"), out=c["out"],
-                                 chunk_rows=c["w"].chunk_rows, on_chunk=on_chunk, stream=stream)
-
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, args.e2e_steps))
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        assert mo.check() == mz.MOSAIC_OK
-        e2e = {"value": world * tot_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "steps": n_e2e}
+        e2e = bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream)
 
     hbm, bf16, bf16_sus, peak_src = load_peaks()
     kernel_tflops = tot_flops * args.steps / (kernel_ms * 1e-3) / 1e12
@@ -364,11 +431,15 @@ def bench_cuda(args):
                    "M": [c["mask"].M for c in calls],
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "gbs": gbs,
+        "member_ms": dict(zip([c["w"].name for c in calls], member_ms)),
+        "kernel_source_hash": kernel_source_hash(),
         "roofline_frac_of_step": roof_time / (ms_per_step * 1e-3) if world == 1 else None,
         "roofline": {
             "bound": "tensor" if tot_flops / (bf16 * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm",
             "achieved": kernel_tflops, "peak": bf16, "unit": "TFLOP/s",
-            "frac": kernel_tflops / bf16, "traffic": args.traffic,
+            "frac": kernel_tflops / bf16,
+            "traffic": (args.traffic if args.traffic is not None
+                        else MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(args.workload)),
             "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback 1.9 PFLOP/s",
             "kernel": "gather_gemm_kernel<false>", "achieved_gbs": tot_bytes * args.steps / (kernel_ms * 1e-3) / 1e9,
             "hbm_peak_gbs": hbm,

@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py that needs no GPU: the cross-rank max used for timing (run as a
+world-size-2 gloo job on CPU), per-rank seeds, algorithmic byte counts, the kernel-source hash
+and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        vals = [1.0 + rank, 10.0 - rank, 5.0 * rank]
+        q.put((rank, bench.max_over_ranks(vals, torch.device("cpu")), bench.rank_seed_shift(rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 2000)
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0][1] == res[1][1] == [2.0, 10.0, 5.0]
+    assert res[0][2] != res[1][2]  # independent batches per rank
+
+
+def test_max_over_ranks_single_process_is_identity():
+    assert bench.max_over_ranks([3.0, 1.5], torch.device("cpu")) == [3.0, 1.5]
+
+
+def test_algorithmic_bytes_llada_r05():
+    # W once + gathered rows once + bf16 logits once + int32 indices
+    assert bench.algorithmic_bytes(2048, 126464, 4096, 2) == (
+        2 * 126464 * 4096 + 2 * 2048 * 4096 + 2 * 2048 * 126464 + 4 * 2048)
+
+
+def test_kernel_source_hash_is_stable():
+    assert bench.kernel_source_hash() == bench.kernel_source_hash()
+    assert len(bench.kernel_source_hash()) == 16
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1", "--ref-step-s", "0.2"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["unit"] == "TFLOP/s" and j["higher_is_better"]
+    assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
+
+
+def test_reference_arm_non_zero_rank_exits_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
