@@ -9,11 +9,13 @@
 // buffer is ever written. The pages' kernel targeted RTX 3090 / A100; this one is designed for
 // Blackwell instead.
 //
-// Roles (per CTA, 320 threads):
+// Roles (per CTA, 352 threads):
 //   warps 6..9  A gather: each of the 128 threads resolves 8 of the tile's mask indices to
 //               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
 //               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
 //               a STAGES-deep shared-memory ring (8 threads cover one 128-byte row segment).
+//   warp 10     relay: when a stage's gathered rows have landed, fences them into the async
+//               proxy and reports the stage to the (leader's) full barrier.
 //   warp 0      W stream: one thread issues a 2-D TMA load of the W tile per K block.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
 //               accumulator (2 x 256 fp32 columns) and commits stage releases.
@@ -27,8 +29,7 @@
 // SM takes in 32 KiB per K block instead of 48 KiB; per-SM ingress was the measured limit of
 // the single-CTA 128 x 256 form. The leader's stage barriers collect the whole pair: its W
 // expect_tx covers both halves (each CTA's cta_group::2 TMA load reports its bytes there), and
-// an otherwise idle thread of the peer relays the peer's gather completions with one
-// cluster-scope arrive per K block. Commits multicast to both CTAs. PAIR = false runs
+// each CTA's relay reports its own gathered rows. Commits multicast to both CTAs. PAIR = false runs
 // 128 x 256 tiles on one CTA (problems with a single M tile).
 //
 // The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
@@ -66,7 +67,8 @@ constexpr int EPI_THREADS = 128;
 constexpr int A_WARP0 = 6;
 constexpr int A_WARPS = 4;
 constexpr int A_THREADS = 32 * A_WARPS;
-constexpr int NUM_THREADS = (A_WARP0 * 32) + A_THREADS;  // 320
+constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 10
+constexpr int NUM_THREADS = (RELAY_WARP + 1) * 32;  // 352
 constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
 
 template <bool PAIR>
@@ -84,11 +86,11 @@ struct Cfg {
   // misc: tmem slot, abort flag, epilogue verdict, pad; 16-byte relay signal slot
   static constexpr int SMEM_OFFS_OFF = SMEM_MISC_OFF + 32;  // seq_offsets, mask_offsets copies
   static constexpr int SMEM_BYTES = SMEM_OFFS_OFF + 2 * OFFS_CAP * 4 + 1024;  // + alignment slack
-  // Arrivals per phase on the (leader's) full barrier: its expect_tx and one per local gather
-  // thread (made by the hardware when that thread's copies have landed). The bytes it expects:
-  // W of both CTAs and, for a pair, the 16-byte signal with which the peer reports that its
-  // gathered rows have landed. On the (leader's) tempty barrier: one arrive per CTA.
-  static constexpr int FULL_COUNT = 1 + A_THREADS;
+  // Arrivals per phase on the (leader's) full barrier: its W expect_tx and its relay's arrive
+  // (the local gathered rows have landed and are fenced). The bytes it expects: W of both CTAs
+  // and, for a pair, the 16-byte signal with which the peer's relay reports the peer's rows. On
+  // the (leader's) tempty barrier: one arrive per CTA.
+  static constexpr int FULL_COUNT = 2;
   static constexpr int TEMPTY_COUNT = PAIR ? 2 : 1;
   static constexpr int SIGNAL_BYTES = 16;
   static constexpr uint32_t W_TX = (PAIR ? 2 : 1) * B_STAGE + (PAIR ? SIGNAL_BYTES : 0);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(sm.full(s), C::FULL_COUNT);  // used in the leader (or the single CTA)
       mbar_init(sm.empty(s), 1);             // MMA commit (multicast to both CTAs of a pair)
-      mbar_init(sm.afull(s), A_THREADS);     // peer of a pair: its gather threads, for the relay
+      mbar_init(sm.afull(s), A_THREADS);     // gather threads (hardware arrive on landing)
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(sm.tfull(j), 1);                 // MMA commit
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= A_WARP0) {
+  } else if (warp >= A_WARP0 && warp < RELAY_WARP) {
     // ---------------------------------------------------------------- A gather (cp.async)
     const int at = threadIdx.x - A_WARP0 * 32;  // 0..127
     const int chunk = at & 7;                   // 16-byte piece of a 128-byte row segment
@@ -353,34 +355,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           cp_async_16(dst, live ? src[j] + static_cast<int64_t>(kb) * (BK * 2) : hbase,
                       live ? 16u : 0u, pol_a);
         }
-        // Publish without waiting: the arrive happens when these copies have landed. The
-        // consumer of the stage fences them into the async proxy before the tensor cores read.
-        cp_async_arrive_noinc(leader ? sm.full(stage) : sm.afull(stage));
+        // Publish without waiting: the arrive on afull happens when these copies have landed;
+        // the relay then fences them into the async proxy for the tensor cores.
+        cp_async_arrive_noinc(sm.afull(stage));
         ++it;
       }
     }
     cp_async_wait<0>();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (PAIR && !leader && lane == 0) {
-      // Relay (peer CTA of a pair): once this CTA's gather warps have published a stage (their
-      // copies landed and were fenced to the async proxy), report it to the leader's full
-      // barrier through the async proxy: a 16-byte shared-to-shared bulk copy whose complete_tx
-      // lands there. A cluster-scope release arrive instead was measured to cost ~0.8 us per
-      // K block, which capped the pair at ~30 % of the tensor peak.
-      const uint32_t dst = mapa_shared(sm.signal_slot(), 0);
+  } else if (warp == RELAY_WARP) {
+    // ---------------------------------------------------------------- relay
+    if (lane == 0) {
+      // Once a stage's gathered rows have landed (every gather thread's hardware arrive on
+      // afull), fence them into the async proxy and report the stage: in the leader (or a single
+      // CTA) by a local arrive on full; in the peer of a pair through the async proxy, with a
+      // 16-byte shared-to-shared bulk copy whose complete_tx lands on the leader's full barrier
+      // (a cluster-scope release arrive instead cost ~0.8 us per K block). Keeping the fence
+      // here keeps it off the MMA issuer, the kernel's critical thread.
+      const uint32_t dst = PAIR ? mapa_shared(sm.signal_slot(), 0) : 0;
       int stage = 0;
       uint32_t phase = 0;
       bool alive = true;
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
-          fence_proxy_async_smem();  // the landed rows, for the async-proxy (MMA) reads
-          bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
+          fence_proxy_async_smem();
+          if (leader) mbar_arrive(sm.full(stage));
+          else bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
     }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
@@ -394,7 +401,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
-          fence_proxy_async_smem();  // gathered rows were written by cp.async (generic proxy)
           tc_fence_after();
           const uint64_t a0 = smem_desc_sw128(sm.a(stage));
           const uint64_t b0 = smem_desc_sw128(sm.b(stage));
