@@ -133,6 +133,25 @@ MOSAIC_API mosaic_status mosaic_set_wait_timeout(mosaic_handle* handle, uint64_t
 /* Number of kernel launches enqueued through this handle since creation. */
 MOSAIC_API int64_t mosaic_launch_count(const mosaic_handle* handle);
 
+/*
+ * Lazy chunking's "minimum sufficient chunk count" for the logits output
+ * ("扩散大语言模型内存优化：Mosaic系统突破与实践", section 2.3: chunking stays off unless memory is
+ * short, and then the smallest chunk count that fits is used; paper review section 3, core
+ * component 3). Host-only arithmetic, no GPU needed.
+ *
+ * Given M masked rows, vocabulary V, the output dtype and a byte budget for the live output
+ * buffer, writes to *chunk_rows the value to pass to mosaic_masked_logits and to *n_chunks the
+ * number of launches it gives:
+ *   - M * V * elt <= budget: chunking stays off, *chunk_rows = 0, *n_chunks = (M > 0);
+ *   - otherwise the fewest chunks n whose rows fit (ceil(M / n) * V * elt <= budget), with the
+ *     rows balanced across them: *chunk_rows = ceil(M / n) (the last chunk may be shorter).
+ * MOSAIC_ERR_UNSUPPORTED if not even one row fits; MOSAIC_ERR_INVALID_ARG for M < 0, V < 1,
+ * budget < 0, an unknown dtype or NULL outputs.
+ */
+MOSAIC_API mosaic_status mosaic_min_chunk_rows(int64_t M, int64_t V, mosaic_dtype out_dtype,
+                                               int64_t budget_bytes, int64_t* chunk_rows,
+                                               int64_t* n_chunks);
+
 /* Text of the last error produced on the calling thread ("" if none). */
 MOSAIC_API const char* mosaic_last_error_string(void);
 

@@ -106,6 +106,31 @@ extern "C" {
 
 const char* mosaic_last_error_string(void) { return g_last_error.c_str(); }
 
+mosaic_status mosaic_min_chunk_rows(int64_t M, int64_t V, mosaic_dtype out_dtype,
+                                    int64_t budget_bytes, int64_t* chunk_rows,
+                                    int64_t* n_chunks) {
+  if (!chunk_rows || !n_chunks) return fail(MOSAIC_ERR_INVALID_ARG, "NULL output pointer");
+  if (M < 0 || V < 1 || budget_bytes < 0)
+    return fail(MOSAIC_ERR_INVALID_ARG, "need M >= 0, V >= 1, budget_bytes >= 0");
+  if (out_dtype != MOSAIC_BF16 && out_dtype != MOSAIC_F32)
+    return fail(MOSAIC_ERR_INVALID_ARG, "unknown out_dtype %d", static_cast<int>(out_dtype));
+  const int64_t row_bytes = V * (out_dtype == MOSAIC_F32 ? 4 : 2);
+  const int64_t fit = budget_bytes / row_bytes;  // most rows the budget holds
+  if (M <= fit) {  // everything fits: chunking stays off
+    *chunk_rows = 0;
+    *n_chunks = M > 0 ? 1 : 0;
+    return MOSAIC_OK;
+  }
+  if (fit < 1)
+    return fail(MOSAIC_ERR_UNSUPPORTED, "a budget of %lld bytes holds no output row of %lld bytes",
+                static_cast<long long>(budget_bytes), static_cast<long long>(row_bytes));
+  const int64_t n = (M + fit - 1) / fit;      // fewest chunks whose rows fit
+  const int64_t rows = (M + n - 1) / n;       // balanced: rows <= fit
+  *chunk_rows = rows;
+  *n_chunks = (M + rows - 1) / rows;
+  return MOSAIC_OK;
+}
+
 mosaic_status mosaic_create(mosaic_handle** handle, int device) {
   if (!handle) return fail(MOSAIC_ERR_INVALID_ARG, "handle out-pointer is NULL");
   *handle = nullptr;

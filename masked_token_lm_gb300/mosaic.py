@@ -70,6 +70,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                                  ctypes.c_int, I64, mosaic_chunk_cb, P,
                                                  ctypes.POINTER(ctypes.c_uint32), P]
     lib.mosaic_masked_logits_noalloc.restype = ctypes.c_int
+    lib.mosaic_min_chunk_rows.argtypes = [I64, I64, ctypes.c_int, I64,
+                                          ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int64)]
+    lib.mosaic_min_chunk_rows.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -106,6 +110,14 @@ def mosaic_masked_logits_noalloc(hidden, L_tot, d, mask_idx, M, seq_offsets, mas
                                                        mask_offsets, B, W, V, out, out_dtype,
                                                        chunk_rows, cb_c, user, chunk_status,
                                                        stream)
+
+
+def mosaic_min_chunk_rows(M: int, V: int, out_dtype: int, budget_bytes: int):
+    """Returns (status, chunk_rows, n_chunks): the fewest chunks whose live output fits."""
+    cr, nc = ctypes.c_int64(), ctypes.c_int64()
+    st = load_library().mosaic_min_chunk_rows(int(M), int(V), int(out_dtype), int(budget_bytes),
+                                              ctypes.byref(cr), ctypes.byref(nc))
+    return st, cr.value, nc.value
 
 
 def mosaic_check(handle, stream) -> int:

@@ -31,7 +31,7 @@ def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
         "mosaic_launch_count", "mosaic_masked_logits", "mosaic_masked_logits_noalloc",
-        "mosaic_set_wait_timeout"])
+        "mosaic_min_chunk_rows", "mosaic_set_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol(lib_path):
@@ -80,3 +80,40 @@ def test_product_package_does_not_import_the_oracle():
                 src = open(os.path.join(dp, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from\s+oracle|import\s+oracle)", src, re.M), f
                 assert not re.search(r'#include\s+"[^"]*oracle', src), f
+
+
+def _brute_min_chunks(M, V, elt, budget):
+    if M * V * elt <= budget:
+        return 0, (1 if M > 0 else 0)
+    for n in range(1, M + 1):
+        rows = -(-M // n)
+        if rows * V * elt <= budget:
+            return rows, -(-M // rows)
+    return None
+
+
+def test_min_chunk_rows_matches_brute_force(lib_path):
+    import itertools
+    mosaic.load_library()
+    for M, V, dt, budget in itertools.product([0, 1, 7, 100, 1000, 4097], [1, 8, 1024],
+                                              [mosaic.MOSAIC_BF16, mosaic.MOSAIC_F32],
+                                              [0, 15, 16, 17, 1000, 4096, 10 ** 5, 10 ** 7]):
+        elt = 4 if dt == mosaic.MOSAIC_F32 else 2
+        st, cr, nc = mosaic.mosaic_min_chunk_rows(M, V, dt, budget)
+        want = _brute_min_chunks(M, V, elt, budget)
+        if want is None:
+            assert st == mosaic.MOSAIC_ERR_UNSUPPORTED, (M, V, dt, budget)
+            continue
+        assert st == mosaic.MOSAIC_OK, (M, V, dt, budget, mosaic.mosaic_last_error_string())
+        assert (cr, nc) == want, (M, V, dt, budget, cr, nc, want)
+        if cr:
+            assert cr * V * elt <= budget and nc == -(-M // cr)
+
+
+def test_min_chunk_rows_long_context_budget(lib_path):
+    # 117,965 rows x 126,464 bf16 = 29.8 GB; a 1.036 GB budget (4096 rows) needs 29 chunks
+    st, cr, nc = mosaic.mosaic_min_chunk_rows(117965, 126464, mosaic.MOSAIC_BF16, 4096 * 126464 * 2)
+    assert st == mosaic.MOSAIC_OK and nc == 29 and cr <= 4096 and cr * 29 >= 117965
+    st, cr, nc = mosaic.mosaic_min_chunk_rows(2048, 126464, mosaic.MOSAIC_BF16, 10 ** 12)
+    assert (st, cr, nc) == (mosaic.MOSAIC_OK, 0, 1)  # lazy: off when it fits
+    assert mosaic.mosaic_min_chunk_rows(-1, 8, 0, 10)[0] == mosaic.MOSAIC_ERR_INVALID_ARG

@@ -111,6 +111,26 @@ def test_csr_ragged_with_empty_sequences(mo):
     assert_close(out, ref, torch.bfloat16, "csr ragged")
 
 
+def test_csr_many_sequences_offsets_from_global_memory(mo):
+    # B = 200 > 128: the kernel searches the offsets in global memory instead of shared memory
+    g = np.random.default_rng(12)
+    B = 200
+    Ls = g.integers(1, 40, B)
+    counts = np.minimum(Ls, g.integers(0, 6, B))
+    counts[::17] = 0  # some empty sequences
+    so = np.concatenate([[0], np.cumsum(Ls)]).astype(np.int32)
+    moff = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    idx = np.concatenate([np.sort(g.choice(L, c, replace=False)) for L, c in zip(Ls, counts)]).astype(np.int32)
+    d, V = 128, 520
+    H, W = rand_inputs(int(so[-1]), d, V, seed=13)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = run(mo, H, t(idx), W, torch.float32, t(so), t(moff))
+    ref = orc.masked_logits(bits(H), idx, bits(W), so, moff)
+    assert_close(out, ref, torch.float32, "csr B=200")
+    flat = run(mo, H, t(orc.resolve_rows(idx, int(so[-1]), so, moff).astype(np.int32)), W, torch.float32)
+    assert torch.equal(out, flat)
+
+
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
 def test_one_hot_hidden_is_bit_exact(mo, dt):
     # H[r, :] = e_(r mod d): out[i, v] = W[v, row(i) mod d] exactly, in any dtype.
@@ -245,3 +265,15 @@ def test_bounded_wait_timeout_reports_and_context_survives(mo):
     out = run(mo, H[:256], idx[:100] % 256, W[:1024], torch.float32)
     ref = orc.masked_logits(bits(H[:256]), (idx[:100] % 256).cpu().numpy(), bits(W[:1024]))
     assert_close(out, ref, torch.float32, "after timeout")
+
+
+def test_min_chunk_rows_drives_a_chunked_call_within_budget(mo):
+    # lazy chunking with the minimum sufficient chunk count for a 250-row output budget
+    L, d, V, M = 2000, 256, 1032, 900
+    H, W = rand_inputs(L, d, V, seed=51)
+    idx = wl.uniform_positions(L, M, seed=52).to(DEV)
+    st, cr, nc = mz.mosaic_min_chunk_rows(M, V, mz.MOSAIC_BF16, 250 * V * 2 + 100)
+    assert (st, cr, nc) == (mz.MOSAIC_OK, 225, 4)
+    full = run(mo, H, idx, W, torch.bfloat16)
+    chunked = run(mo, H, idx, W, torch.bfloat16, chunk_rows=cr)
+    assert torch.equal(full.view(torch.int16), chunked.view(torch.int16))
