@@ -11,6 +11,8 @@ from .mask_only_logits import (  # noqa: F401
     logits_bytes,
     masked_logits,
     masked_logits_chunked,
+    masked_sample,
+    sample_from_logits,
     resolve_rows,
     round_output,
 )

@@ -204,3 +204,30 @@ def masked_logits_chunked(H_bits, idx, W_bits, seq_offsets=None, mask_offsets=No
 def logits_bytes(rows: int, V: int, elt_bytes: int) -> int:
     """Bytes of a [rows, V] logit tensor with ``elt_bytes`` bytes per element."""
     return int(rows) * int(V) * int(elt_bytes)
+
+
+# ---------------------------------------------------------------------------------------------
+# Sampling the masked positions (the step after mask-only logits).
+# ---------------------------------------------------------------------------------------------
+
+def sample_from_logits(logits: np.ndarray):
+    """Greedy token and its confidence for each row of a [M, V] logit matrix.
+
+    "Mosaic: Unlocking Long-Context Inference for Diffusion LLMs via Global Memory" (paper review),
+    section 3, observation #2: only the masked tokens are sampled. Reading (the pages give no
+    sampler): greedy decoding, token = argmax_v logits[i, v] with ties going to the smallest v,
+    and confidence = the softmax probability of that token, max_v softmax(logits[i])_v =
+    1 / sum_v exp(logits[i, v] - max_v logits[i, v]). Returns (int64 [M], float64 [M]).
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    if z.shape[0] == 0:
+        return np.zeros(0, np.int64), np.zeros(0, np.float64)
+    token = np.argmax(z, axis=1)  # numpy returns the first occurrence of the maximum
+    zmax = z[np.arange(z.shape[0]), token]
+    conf = 1.0 / np.sum(np.exp(z - zmax[:, None]), axis=1)
+    return token.astype(np.int64), conf
+
+
+def masked_sample(H_bits, idx, W_bits, seq_offsets=None, mask_offsets=None):
+    """Token and confidence of every masked position: sampling applied to mask-only logits."""
+    return sample_from_logits(masked_logits(H_bits, idx, W_bits, seq_offsets, mask_offsets))

@@ -304,3 +304,53 @@ def test_ragged_mask_structure():
     assert len(set(counts)) > 1  # ragged
     rows = orc.resolve_rows(m.idx.numpy(), 8000, m.seq_offsets.numpy(), m.mask_offsets.numpy())
     assert np.all(np.diff(rows) > 0)
+
+
+# ------------------------------------------------------------------ sampling the masked rows
+
+def test_sample_closed_forms():
+    # all logits equal: token 0 (first), confidence 1/V
+    t, c = orc.sample_from_logits(np.zeros((3, 7)))
+    assert t.tolist() == [0, 0, 0] and np.allclose(c, 1 / 7, rtol=0, atol=1e-15)
+    # two-way tie at the top: the smaller index wins; confidence from the definition by hand
+    z = np.array([[0.0, 2.0, -1.0, 2.0]])
+    t, c = orc.sample_from_logits(z)
+    assert t.tolist() == [1]
+    assert abs(c[0] - 1.0 / (np.exp(-2.0) + 1 + np.exp(-3.0) + 1)) < 1e-15
+    # a dominant logit: confidence tends to 1
+    t, c = orc.sample_from_logits(np.array([[0.0, 50.0, 0.0]]))
+    assert t.tolist() == [1] and 1 - c[0] < 1e-20
+    assert orc.sample_from_logits(np.zeros((0, 5)))[0].shape == (0,)
+
+
+def test_sample_confidence_matches_logsumexp_library():
+    from scipy.special import logsumexp
+
+    z = rng.standard_normal((50, 300)) * 3
+    t, c = orc.sample_from_logits(z)
+    assert np.array_equal(t, np.argmax(z, axis=1))
+    np.testing.assert_allclose(np.log(c), z.max(axis=1) - logsumexp(z, axis=1), rtol=0, atol=1e-12)
+
+
+def test_sample_integer_inputs_exact_argmax():
+    L, d, V = 30, 256, 77
+    Hi, Wi = rng.integers(-2, 3, (L, d)), rng.integers(-2, 3, (V, d))
+    to_b = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    idx = np.array([3, 0, 29, 3, 11], np.int32)
+    t, c = orc.masked_sample(to_b(Hi), idx, to_b(Wi))
+    exact = Hi[idx] @ Wi.T
+    first = np.array([int(np.flatnonzero(row == row.max())[0]) for row in exact])
+    assert np.array_equal(t, first)
+    want = np.array([1.0 / sum(np.exp(float(v - row.max())) for v in row) for row in exact])
+    np.testing.assert_allclose(c, want, rtol=1e-14)
+
+
+def test_sample_one_hot_picks_the_weight_column_maximum():
+    L, d, V = 40, 32, 50
+    Hf = np.zeros((L, d)); Hf[np.arange(L), np.arange(L) % d] = 1
+    H = torch.from_numpy(Hf.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    W = rand_bf16((V, d), 0.02)
+    idx = np.array([0, 5, 33, 39], np.int32)
+    t, _ = orc.masked_sample(H, idx, W)
+    Wf = orc.bf16_bits_to_f64(W)
+    assert t.tolist() == [int(np.argmax(Wf[:, r % d])) for r in idx]
