@@ -103,6 +103,12 @@ def rank_seed_shift(rank):
     return 100000 * rank
 
 
+def sample_bytes(M, V, d, ws_bytes):
+    """Fused sampling: W once + gathered rows once + the partials written and read back once +
+    token and confidence (the [M, V] logits are never written)."""
+    return 2 * V * d + 2 * M * d + 2 * ws_bytes + 8 * M + 4 * M
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -355,9 +361,15 @@ def bench_cuda(args):
         odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
         chunked = 0 < w.chunk_rows < mask.M
         out = torch.empty((w.chunk_rows if chunked else mask.M, w.V), dtype=odt, device=dev)
-        calls.append(dict(w=w, mask=mask, H=H, W=W, out=out, odt=odt, chunked=chunked))
+        call = dict(w=w, mask=mask, H=H, W=W, out=out, odt=odt, chunked=chunked)
+        if args.mode == "sample":
+            ws_bytes = mz.mosaic_masked_sample_workspace_bytes(mask.M, w.V, w.chunk_rows)
+            call["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+            tot_bytes += sample_bytes(mask.M, w.V, w.d, ws_bytes)
+        else:
+            tot_bytes += algorithmic_bytes(mask.M, w.V, w.d, out.element_size())
+        calls.append(call)
         tot_flops += w.flops(mask.M)
-        tot_bytes += algorithmic_bytes(mask.M, w.V, w.d, out.element_size())
     # identical W across members of one workload set: share it
     for c in calls[1:]:
         if c["w"].V == calls[0]["w"].V and c["w"].d == calls[0]["w"].d:
@@ -367,6 +379,10 @@ def bench_cuda(args):
 
     def one_call(c):
         m = c["mask"]
+        if args.mode == "sample":
+            mo.masked_sample(c["H"], m.idx, c["W"], m.seq_offsets, m.mask_offsets,
+                             chunk_rows=c["w"].chunk_rows, workspace=c["workspace"], stream=stream)
+            return
         mo.masked_logits(c["H"], m.idx, c["W"], m.seq_offsets, m.mask_offsets, out=c["out"],
                          chunk_rows=c["w"].chunk_rows, on_chunk=noop if c["chunked"] else None,
                          stream=stream)
@@ -417,7 +433,7 @@ def bench_cuda(args):
 
     # ---- end to end through the public call: pinned host inputs -> device -> logits -> host
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.mode == "logits":
         e2e = bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream)
 
     hbm, bf16, bf16_sus, peak_src = load_peaks()
@@ -432,6 +448,7 @@ def bench_cuda(args):
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "gbs": gbs,
         "member_ms": dict(zip([c["w"].name for c in calls], member_ms)),
+        "mode": args.mode,
         "kernel_source_hash": kernel_source_hash(),
         "roofline_frac_of_step": roof_time / (ms_per_step * 1e-3) if world == 1 else None,
         "roofline": {
@@ -469,6 +486,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llada8b")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--mode", default="logits", choices=["logits", "sample"],
+                    help="logits: [M, V] mask-only logits (the metric); sample: fused greedy "
+                         "sampling (token + confidence per masked row)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

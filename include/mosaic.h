@@ -134,6 +134,34 @@ MOSAIC_API mosaic_status mosaic_set_wait_timeout(mosaic_handle* handle, uint64_t
 MOSAIC_API int64_t mosaic_launch_count(const mosaic_handle* handle);
 
 /*
+ * Greedy sampling of the masked positions, fused with the mask-only logits: the step that
+ * follows the logits in a denoising step (paper review, section 3, observation #2: only the
+ * masked tokens are sampled). The [M, V] logits are never written; per masked position i:
+ *
+ *     token[i]      = argmax_v logits[i, v]          (ties: the smallest v)
+ *     confidence[i] = max_v softmax(logits[i, :])_v  = 1 / sum_v exp(logits[i, v] - max)
+ *
+ * computed from the fp32 accumulators. Arguments as for mosaic_masked_logits, plus:
+ * token       int32 [M], device; confidence fp32 [M], device (4-byte aligned).
+ * workspace   device scratch of at least mosaic_masked_sample_workspace_bytes(M, V, chunk_rows)
+ *             bytes, 16-byte aligned, owned by the caller (per-tile partial maxima, sums and
+ *             arguments); chunk_rows (same rule as mosaic_masked_logits) only bounds its size.
+ * A position whose mask index is bad gets token -1 and confidence 0 (and the status word is
+ * set, see mosaic_check). Two kernel launches per chunk (the fused gather-GEMM and a per-row
+ * reduction over the N tiles); results are deterministic.
+ */
+MOSAIC_API int64_t mosaic_masked_sample_workspace_bytes(int64_t M, int64_t V, int64_t chunk_rows);
+MOSAIC_API mosaic_status mosaic_masked_sample(mosaic_handle* handle,
+                                              const void* hidden, int64_t L_tot, int64_t d,
+                                              const int32_t* mask_idx, int64_t M,
+                                              const int32_t* seq_offsets,
+                                              const int32_t* mask_offsets, int32_t B,
+                                              const void* W, int64_t V,
+                                              int32_t* token, float* confidence,
+                                              void* workspace, int64_t workspace_bytes,
+                                              int64_t chunk_rows, void* stream);
+
+/*
  * Lazy chunking's "minimum sufficient chunk count" for the logits output
  * ("扩散大语言模型内存优化：Mosaic系统突破与实践", section 2.3: chunking stays off unless memory is
  * short, and then the smallest chunk count that fits is used; paper review section 3, core

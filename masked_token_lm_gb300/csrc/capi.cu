@@ -24,6 +24,7 @@ struct mosaic_handle {
   int device = 0;
   int num_sms = 0;
   int max_clusters[2][2] = {};  // [out_f32][pair]: clusters resident at once
+  int max_clusters_sample[2] = {};  // [pair], sampling epilogue
   uint32_t* d_status = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int64_t launches = 0;
@@ -155,6 +156,14 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
       delete h;
       return cuda_fail(e, "kernel attributes / cluster occupancy");
     }
+  }
+  for (int pair = 0; pair < 2 && e == cudaSuccess; ++pair) {
+    e = mosaic::gather_gemm_prepare_sample(pair != 0, &h->max_clusters_sample[pair]);
+    if (e == cudaSuccess && h->max_clusters_sample[pair] < 1) e = cudaErrorInvalidConfiguration;
+  }
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e, "sampling kernel attributes / cluster occupancy");
   }
   e = cudaMalloc(&h->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 256);
@@ -290,6 +299,110 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     ++h->launches;
     if (cb) cb(c, rb, rows, out, user);
+  }
+  return MOSAIC_OK;
+}
+
+int64_t mosaic_masked_sample_workspace_bytes(int64_t M, int64_t V, int64_t chunk_rows) {
+  if (M < 0 || V < 1) return -1;
+  const int64_t cr = (chunk_rows > 0 && chunk_rows < M) ? chunk_rows : M;
+  const int64_t n_tiles = (V + mosaic::gather_gemm_block_n() - 1) / mosaic::gather_gemm_block_n();
+  const int64_t ld = (n_tiles + 3) / 4 * 4;  // partials of one row, 16-byte aligned
+  return 3 * cr * ld * 4;
+}
+
+mosaic_status mosaic_masked_sample(mosaic_handle* h, const void* hidden, int64_t L_tot, int64_t d,
+                                   const int32_t* mask_idx, int64_t M,
+                                   const int32_t* seq_offsets, const int32_t* mask_offsets,
+                                   int32_t B, const void* W, int64_t V, int32_t* token,
+                                   float* confidence, void* workspace, int64_t workspace_bytes,
+                                   int64_t chunk_rows, void* stream_ptr) {
+  if (!h) return fail(MOSAIC_ERR_INVALID_ARG, "NULL handle");
+  if (M < 0) return fail(MOSAIC_ERR_INVALID_ARG, "M < 0");
+  if (M >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "M >= 2^31");
+  if ((seq_offsets == nullptr) != (mask_offsets == nullptr))
+    return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs both seq_offsets and mask_offsets");
+  const bool csr = seq_offsets != nullptr;
+  if (csr && B < 1) return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs B >= 1");
+  if (M == 0) return MOSAIC_OK;
+  if (!hidden || !W || !mask_idx || !token || !confidence || !workspace)
+    return fail(MOSAIC_ERR_INVALID_ARG, "NULL hidden, W, mask_idx, token, confidence or workspace");
+  if (d < 1 || V < 1 || L_tot < 1) return fail(MOSAIC_ERR_INVALID_ARG, "d, V and L_tot must be >= 1");
+  if (d % 8 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 8 (16-byte rows)");
+  if (L_tot >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "L_tot >= 2^31");
+  if (V >= (1ll << 31) || d >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "V or d too large");
+  if (!aligned16(hidden) || !aligned16(W) || !aligned16(workspace))
+    return fail(MOSAIC_ERR_INVALID_ARG, "hidden, W and workspace must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(token) & 3u) || (reinterpret_cast<uintptr_t>(confidence) & 3u))
+    return fail(MOSAIC_ERR_INVALID_ARG, "token and confidence must be 4-byte aligned");
+  const int64_t need = mosaic_masked_sample_workspace_bytes(M, V, chunk_rows);
+  if (workspace_bytes < need)
+    return fail(MOSAIC_ERR_INVALID_ARG, "workspace of %lld bytes, %lld needed",
+                static_cast<long long>(workspace_bytes), static_cast<long long>(need));
+  cudaError_t e = cudaSetDevice(h->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  if (!is_device_ptr(hidden, h->device) || !is_device_ptr(W, h->device) ||
+      !is_device_ptr(mask_idx, h->device) || !is_device_ptr(token, h->device) ||
+      !is_device_ptr(confidence, h->device) || !is_device_ptr(workspace, h->device) ||
+      (csr && (!is_device_ptr(seq_offsets, h->device) || !is_device_ptr(mask_offsets, h->device))))
+    return fail(MOSAIC_ERR_INVALID_ARG, "every array must be device memory of device %d", h->device);
+
+  const int BM = mosaic::gather_gemm_block_m(), BN = mosaic::gather_gemm_block_n(),
+            BK = mosaic::gather_gemm_block_k();
+  const bool chunked = chunk_rows > 0 && chunk_rows < M;
+  const int64_t cr = chunked ? chunk_rows : M;
+  const int64_t n_tiles = (V + BN - 1) / BN;
+  const int64_t m_tiles_max = (cr + BM - 1) / BM;
+  if (m_tiles_max * n_tiles >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "too many tiles");
+  const bool pair = m_tiles_max >= 2;
+  const int cm = pair ? 2 : 1;
+  CUtensorMap tm_w;
+  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d,
+                 mosaic::gather_gemm_w_box_rows(pair), BK))
+    return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
+  const int64_t ld = (n_tiles + 3) / 4 * 4;
+  float* part_max = static_cast<float*>(workspace);
+  float* part_sum = part_max + cr * ld;
+  int32_t* part_arg = reinterpret_cast<int32_t*>(part_sum + cr * ld);
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t n_chunks = (M + cr - 1) / cr;
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int64_t rb = c * cr;
+    const int64_t rows = (M - rb < cr) ? (M - rb) : cr;
+    mosaic::GatherGemmParams p = {};
+    p.hidden = hidden;
+    p.idx = mask_idx;
+    p.seq_offsets = csr ? seq_offsets : nullptr;
+    p.mask_offsets = csr ? mask_offsets : nullptr;
+    p.L_tot = L_tot;
+    p.B = csr ? B : 0;
+    p.M_total = static_cast<int32_t>(M);
+    p.row_begin = static_cast<int32_t>(rb);
+    p.rows = static_cast<int32_t>(rows);
+    p.chunk_index = static_cast<int32_t>(c);
+    p.V = static_cast<int32_t>(V);
+    p.d = static_cast<int32_t>(d);
+    p.k_blocks = static_cast<int32_t>((d + BK - 1) / BK);
+    p.m_tiles = static_cast<int32_t>((rows + BM - 1) / BM);
+    p.n_tiles = static_cast<int32_t>(n_tiles);
+    p.cluster_m = cm;
+    p.m_units = (p.m_tiles + cm - 1) / cm;
+    p.group_u = pick_group_u(p.m_units, cm, d);
+    p.status = h->d_status;
+    p.timeout_ns = h->timeout_ns;
+    p.part_max = part_max;
+    p.part_sum = part_sum;
+    p.part_arg = part_arg;
+    p.part_ld = static_cast<int32_t>(ld);
+    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
+    const int64_t clusters = h->max_clusters_sample[pair ? 1 : 0];
+    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
+    e = mosaic::gather_gemm_launch_sample(tm_w, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM (sampling) launch");
+    e = mosaic::sample_reduce_launch(p, token, confidence, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "sampling reduction launch");
+    h->launches += 2;
   }
   return MOSAIC_OK;
 }

@@ -207,7 +207,7 @@ __device__ __forceinline__ TileCoord unit_coord(int u, int rank, const GatherGem
   return c;
 }
 
-template <bool OUT_F32, bool PAIR>
+template <bool OUT_F32, bool PAIR, bool SAMPLE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_out,
@@ -449,54 +449,89 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
       const int n0 = tc.n * BN;
-      for (int c = 0; c < CHUNKS; ++c) {
-        uint32_t packed[32];
-        if constexpr (OUT_F32) {
-          tmem_ld_32x32b_x32(t_acc + c * 32, packed);
+      if constexpr (SAMPLE) {
+        // Sampling epilogue: this row's running max, first argmax and sum of exp(x - max) over
+        // the tile's valid columns (fp32 logits straight from TMEM), merged chunk by chunk.
+        float m = -INFINITY, s = 0.0f;
+        int a = 0;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_acc + c * 32, v);
           tmem_wait_ld();
-          if (!ok) {
+          const int col0 = n0 + c * 32;
+          float cm = -INFINITY;
+          int ca = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) packed[j] = 0u;
+          for (int j = 0; j < 32; ++j) {
+            const float x = __uint_as_float(v[j]);
+            if (col0 + j < p.V && x > cm) { cm = x; ca = col0 + j; }
           }
-        } else {
-          uint32_t v0[32], v1[32];
-          tmem_ld_32x32b_x32(t_acc + c * 64, v0);
-          tmem_ld_32x32b_x32(t_acc + c * 64 + 32, v1);
-          tmem_wait_ld();
+          if (cm > m) { s *= __expf(m - cm); m = cm; a = ca; }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            packed[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
-            packed[16 + j] =
-                pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
-          }
-          if (!ok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) packed[j] = 0u;
-          }
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < p.V) s += __expf(__uint_as_float(v[j]) - m);
         }
-        if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
-        // The staging buffer is free once the store issued from it two chunks ago has read it.
-        if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
-        named_bar_sync(1, EPI_THREADS);
-        if (c == CHUNKS - 1 && et == 0) {
-          // All columns of this accumulator are in registers: hand it back to the MMA issuer.
-          if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
-        }
-        const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
-        const int sw = row_in_tile & 7;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          st_shared_v4(dst + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                       packed[4 * j + 3]);
-        }
-        fence_proxy_async_smem();
+        tc_fence_before();  // this thread's TMEM reads are done
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
-          const int x = n0 + c * COLS_PER_CHUNK;
-          if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
-          bulk_commit_group();
+          if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
         }
-        buf ^= 1;
+        if (r < p.rows && tc.m < p.m_tiles) {
+          const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.n;
+          p.part_max[o] = m;
+          p.part_sum[o] = s;
+          p.part_arg[o] = ok ? a : -1;
+        }
+      } else {
+        for (int c = 0; c < CHUNKS; ++c) {
+          uint32_t packed[32];
+          if constexpr (OUT_F32) {
+            tmem_ld_32x32b_x32(t_acc + c * 32, packed);
+            tmem_wait_ld();
+            if (!ok) {
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) packed[j] = 0u;
+            }
+          } else {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(t_acc + c * 64, v0);
+            tmem_ld_32x32b_x32(t_acc + c * 64 + 32, v1);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              packed[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+              packed[16 + j] =
+                  pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+            }
+            if (!ok) {
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) packed[j] = 0u;
+            }
+          }
+          if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
+          // The staging buffer is free once the store issued from it two chunks ago has read it.
+          if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
+          named_bar_sync(1, EPI_THREADS);
+          if (c == CHUNKS - 1 && et == 0) {
+            // All columns of this accumulator are in registers: hand it back to the MMA issuer.
+            if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
+          }
+          const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
+          const int sw = row_in_tile & 7;
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            st_shared_v4(dst + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                         packed[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, EPI_THREADS);
+          if (et == 0) {
+            const int x = n0 + c * COLS_PER_CHUNK;
+            if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
+            bulk_commit_group();
+          }
+          buf ^= 1;
+        }
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
@@ -533,23 +568,59 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
   return cfg;
 }
 
-template <bool F32, bool PAIR>
+template <bool F32, bool PAIR, bool SAMPLE = false>
 cudaError_t prepare_one(int* clusters) {
-  cudaError_t e = cudaFuncSetAttribute(gather_gemm_kernel<F32, PAIR>,
+  cudaError_t e = cudaFuncSetAttribute(gather_gemm_kernel<F32, PAIR, SAMPLE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<PAIR>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<F32, PAIR>((PAIR ? 2 : 1) * 64, nullptr, attr);
-  return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR>, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR, SAMPLE>, &cfg);
 }
 
-template <bool F32, bool PAIR>
+template <bool F32, bool PAIR, bool SAMPLE = false>
 cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                        const GatherGemmParams& p, int grid, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<F32, PAIR>(grid, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gather_gemm_kernel<F32, PAIR>, tm_w, tm_out, p);
+  return cudaLaunchKernelEx(&cfg, gather_gemm_kernel<F32, PAIR, SAMPLE>, tm_w, tm_out, p);
+}
+
+// One warp per row: lane l combines the row's partials of N tiles l, l + 32, ... (partials are
+// stored row by row, so the warp's reads are contiguous), then the warp combines the lanes. The
+// maximum goes to the smallest column among equal values (columns of different tiles are
+// disjoint and ordered like the tiles), so ties go to the smallest v; the order of the sums is
+// fixed, so results do not depend on chunking or timing.
+__global__ void sample_reduce_kernel(const GatherGemmParams p, int32_t* token, float* confidence) {
+  const int lane = threadIdx.x & 31;
+  const int r = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (r >= p.rows) return;  // whole warps leave together
+  const float* pm = p.part_max + static_cast<int64_t>(r) * p.part_ld;
+  const float* ps = p.part_sum + static_cast<int64_t>(r) * p.part_ld;
+  const int32_t* pa = p.part_arg + static_cast<int64_t>(r) * p.part_ld;
+  float m = -INFINITY;
+  int a = 0x7fffffff;
+  bool bad = false;
+  for (int n = lane; n < p.n_tiles; n += 32) {
+    const float x = pm[n];
+    const int g = pa[n];
+    bad |= g < 0;
+    if (x > m || (x == m && g < a)) { m = x; a = g; }
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float xo = __shfl_xor_sync(0xffffffffu, m, off);
+    const int go = __shfl_xor_sync(0xffffffffu, a, off);
+    if (xo > m || (xo == m && go < a)) { m = xo; a = go; }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  float s = 0.0f;
+  for (int n = lane; n < p.n_tiles; n += 32) s += ps[n] * expf(pm[n] - m);
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) {
+    token[p.row_begin + r] = bad ? -1 : a;
+    confidence[p.row_begin + r] = bad ? 0.0f : 1.0f / s;
+  }
 }
 
 }  // namespace
@@ -559,6 +630,25 @@ int gather_gemm_block_n() { return BN; }
 int gather_gemm_block_k() { return BK; }
 int gather_gemm_epi_cols(bool out_f32) { return out_f32 ? 32 : 64; }
 int gather_gemm_w_box_rows(bool pair) { return pair ? Cfg<true>::B_ROWS : Cfg<false>::B_ROWS; }
+
+cudaError_t gather_gemm_prepare_sample(bool pair, int* clusters) {
+  return pair ? prepare_one<false, true, true>(clusters) : prepare_one<false, false, true>(clusters);
+}
+
+cudaError_t gather_gemm_launch_sample(const CUtensorMap& tm_w, const GatherGemmParams& p, int grid,
+                                      cudaStream_t stream) {
+  // the sampling epilogue stores no logits: tm_w stands in for the unused output map
+  return p.cluster_m == 2 ? launch_one<false, true, true>(tm_w, tm_w, p, grid, stream)
+                          : launch_one<false, false, true>(tm_w, tm_w, p, grid, stream);
+}
+
+cudaError_t sample_reduce_launch(const GatherGemmParams& p, int32_t* token, float* confidence,
+                                 cudaStream_t stream) {
+  const int threads = 256;  // 8 rows per block
+  const int blocks = (p.rows + threads / 32 - 1) / (threads / 32);
+  sample_reduce_kernel<<<blocks, threads, 0, stream>>>(p, token, confidence);
+  return cudaGetLastError();
+}
 
 cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters) {
   if (out_f32) return pair ? prepare_one<true, true>(clusters) : prepare_one<true, false>(clusters);

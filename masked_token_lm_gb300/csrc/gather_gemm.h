@@ -31,6 +31,11 @@ struct GatherGemmParams {
   int32_t group_u;              // M units per raster group
   uint32_t* status;             // device status word
   uint64_t timeout_ns;          // bound on any single wait
+  // Sampling epilogue only: per (row, N tile) partials at row * part_ld + n_tile.
+  float* part_max;              // max logit of the row within the N tile
+  float* part_sum;              // sum over the tile's columns of exp(logit - part_max)
+  int32_t* part_arg;            // first column of the maximum (-1: the row's index was bad)
+  int32_t part_ld;
 };
 
 int gather_gemm_block_m();
@@ -40,6 +45,14 @@ int gather_gemm_epi_cols(bool out_f32);
 int gather_gemm_w_box_rows(bool pair);
 // Sets the kernel's shared-memory attribute and reports how many clusters fit at once.
 cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters);
+// Same for the sampling epilogue.
+cudaError_t gather_gemm_prepare_sample(bool pair, int* clusters);
+// Gather-GEMM whose epilogue writes per-tile sampling partials instead of logits.
+cudaError_t gather_gemm_launch_sample(const CUtensorMap& tm_w, const GatherGemmParams& p, int grid,
+                                      cudaStream_t stream);
+// Combine the partials of `rows` rows into token[r] and confidence[r].
+cudaError_t sample_reduce_launch(const GatherGemmParams& p, int32_t* token, float* confidence,
+                                 cudaStream_t stream);
 cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                                const GatherGemmParams& p, bool out_f32, int grid,
                                cudaStream_t stream);

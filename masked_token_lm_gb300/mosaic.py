@@ -74,6 +74,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                           ctypes.POINTER(ctypes.c_int64),
                                           ctypes.POINTER(ctypes.c_int64)]
     lib.mosaic_min_chunk_rows.restype = ctypes.c_int
+    lib.mosaic_masked_sample_workspace_bytes.argtypes = [I64, I64, I64]
+    lib.mosaic_masked_sample_workspace_bytes.restype = ctypes.c_int64
+    lib.mosaic_masked_sample.argtypes = [P, P, I64, I64, P, I64, P, P, I32, P, I64, P, P, P, I64,
+                                         I64, P]
+    lib.mosaic_masked_sample.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -118,6 +123,19 @@ def mosaic_min_chunk_rows(M: int, V: int, out_dtype: int, budget_bytes: int):
     st = load_library().mosaic_min_chunk_rows(int(M), int(V), int(out_dtype), int(budget_bytes),
                                               ctypes.byref(cr), ctypes.byref(nc))
     return st, cr.value, nc.value
+
+
+def mosaic_masked_sample_workspace_bytes(M: int, V: int, chunk_rows: int = 0) -> int:
+    return load_library().mosaic_masked_sample_workspace_bytes(int(M), int(V), int(chunk_rows))
+
+
+def mosaic_masked_sample(handle, hidden, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B, W,
+                         V, token, confidence, workspace, workspace_bytes, chunk_rows,
+                         stream) -> int:
+    """Raw call of the fused gather-GEMM + greedy sampling; pointers are ints or None."""
+    return load_library().mosaic_masked_sample(handle, hidden, L_tot, d, mask_idx, M, seq_offsets,
+                                               mask_offsets, B, W, V, token, confidence,
+                                               workspace, workspace_bytes, chunk_rows, stream)
 
 
 def mosaic_check(handle, stream) -> int:
@@ -211,6 +229,32 @@ class Mosaic:
         if st != MOSAIC_OK:
             raise MosaicError(st, mosaic_last_error_string())
         return out
+
+    def masked_sample(self, hidden, mask_idx, W, seq_offsets=None, mask_offsets=None,
+                      chunk_rows: int = 0, workspace=None, stream=None):
+        """Greedy token (int32 [M]) and confidence (fp32 [M]) of every masked position, without
+        writing the [M, V] logits. ``workspace`` (uint8 device tensor) is allocated with torch if
+        not given."""
+        import torch
+
+        M = int(mask_idx.numel())
+        V, d = int(W.shape[0]), int(W.shape[1])
+        token = torch.empty(M, dtype=torch.int32, device=W.device)
+        conf = torch.empty(M, dtype=torch.float32, device=W.device)
+        need = mosaic_masked_sample_workspace_bytes(M, V, chunk_rows)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
+        csr = seq_offsets is not None
+        st = mosaic_masked_sample(
+            self.handle, hidden.data_ptr(), int(hidden.shape[0]), d,
+            mask_idx.data_ptr() if M > 0 else None, M,
+            seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None,
+            int(seq_offsets.numel()) - 1 if csr else 0, W.data_ptr(), V,
+            token.data_ptr() if M > 0 else None, conf.data_ptr() if M > 0 else None,
+            workspace.data_ptr(), workspace.numel(), int(chunk_rows), self._stream_ptr(stream))
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        return token, conf
 
     def check(self, stream=None) -> int:
         """Synchronise and return the device status (MOSAIC_OK / _INDEX / _TIMEOUT / _CUDA)."""

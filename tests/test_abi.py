@@ -31,7 +31,8 @@ def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
         "mosaic_launch_count", "mosaic_masked_logits", "mosaic_masked_logits_noalloc",
-        "mosaic_min_chunk_rows", "mosaic_set_wait_timeout"])
+        "mosaic_masked_sample", "mosaic_masked_sample_workspace_bytes", "mosaic_min_chunk_rows",
+        "mosaic_set_wait_timeout"])
 
 
 def test_library_loads_and_exports_every_declared_symbol(lib_path):
@@ -117,3 +118,11 @@ def test_min_chunk_rows_long_context_budget(lib_path):
     st, cr, nc = mosaic.mosaic_min_chunk_rows(2048, 126464, mosaic.MOSAIC_BF16, 10 ** 12)
     assert (st, cr, nc) == (mosaic.MOSAIC_OK, 0, 1)  # lazy: off when it fits
     assert mosaic.mosaic_min_chunk_rows(-1, 8, 0, 10)[0] == mosaic.MOSAIC_ERR_INVALID_ARG
+
+
+def test_sample_workspace_bytes(lib_path):
+    mosaic.load_library()
+    # 3 arrays (max, sum, arg) x rows x N tiles of 256 columns (rounded up to 4) x 4 bytes
+    assert mosaic.mosaic_masked_sample_workspace_bytes(3686, 126464, 0) == 3 * 3686 * 496 * 4
+    assert mosaic.mosaic_masked_sample_workspace_bytes(10000, 1000, 4096) == 3 * 4096 * 4 * 4
+    assert mosaic.mosaic_masked_sample_workspace_bytes(-1, 10, 0) == -1
