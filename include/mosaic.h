@@ -180,6 +180,28 @@ MOSAIC_API mosaic_status mosaic_min_chunk_rows(int64_t M, int64_t V, mosaic_dtyp
                                                int64_t budget_bytes, int64_t* chunk_rows,
                                                int64_t* n_chunks);
 
+/*
+ * VMM-backed output workspace for lazy chunking (paper review, section 3, core component 4
+ * "Global Memory Manager"; "扩散大语言模型内存优化：Mosaic系统突破与实践", section 3.1: reserve
+ * virtual addresses up front, bind physical pages as demand grows). A contiguous virtual range
+ * of reserve_bytes is reserved on `device` without physical memory; mosaic_workspace_bind makes
+ * sure the first `bytes` of it are backed (binding more pages only when the demand grows) and
+ * returns its base address, which never changes, so a chunk output buffer can grow to the
+ * largest chunk actually used without reallocation or fragmentation. mosaic_workspace_trim waits
+ * for the device to be idle and unbinds pages beyond keep_bytes (in the units they were bound;
+ * the bound size may stay above keep_bytes). Sizes round up to the allocation granularity
+ * (typically 2 MiB). The bound pages are ordinary device memory of `device` and can be passed
+ * as `out` to mosaic_masked_logits. Not thread-safe per workspace.
+ */
+typedef struct mosaic_workspace mosaic_workspace;
+MOSAIC_API mosaic_status mosaic_workspace_create(mosaic_workspace** ws, int device,
+                                                 int64_t reserve_bytes);
+MOSAIC_API mosaic_status mosaic_workspace_bind(mosaic_workspace* ws, int64_t bytes, void** ptr);
+MOSAIC_API mosaic_status mosaic_workspace_trim(mosaic_workspace* ws, int64_t keep_bytes);
+MOSAIC_API int64_t mosaic_workspace_bound_bytes(const mosaic_workspace* ws);
+MOSAIC_API int64_t mosaic_workspace_reserved_bytes(const mosaic_workspace* ws);
+MOSAIC_API mosaic_status mosaic_workspace_destroy(mosaic_workspace* ws);
+
 /* Text of the last error produced on the calling thread ("" if none). */
 MOSAIC_API const char* mosaic_last_error_string(void);
 

@@ -19,6 +19,7 @@
 
 #include "../../include/mosaic.h"
 #include "gather_gemm.h"
+#include "status.h"
 
 struct mosaic_handle {
   int device = 0;
@@ -33,6 +34,12 @@ struct mosaic_handle {
 namespace {
 
 thread_local std::string g_last_error;
+
+}  // namespace
+
+void mosaic::set_last_error(const char* msg) { g_last_error = msg; }
+
+namespace {
 
 mosaic_status fail(mosaic_status s, const char* fmt, ...) {
   char buf[512];

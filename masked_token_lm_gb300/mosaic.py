@@ -79,6 +79,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mosaic_masked_sample.argtypes = [P, P, I64, I64, P, I64, P, P, I32, P, I64, P, P, P, I64,
                                          I64, P]
     lib.mosaic_masked_sample.restype = ctypes.c_int
+    lib.mosaic_workspace_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, I64]
+    lib.mosaic_workspace_create.restype = ctypes.c_int
+    lib.mosaic_workspace_bind.argtypes = [P, I64, ctypes.POINTER(ctypes.c_void_p)]
+    lib.mosaic_workspace_bind.restype = ctypes.c_int
+    lib.mosaic_workspace_trim.argtypes = [P, I64]
+    lib.mosaic_workspace_trim.restype = ctypes.c_int
+    lib.mosaic_workspace_bound_bytes.argtypes = [P]
+    lib.mosaic_workspace_bound_bytes.restype = ctypes.c_int64
+    lib.mosaic_workspace_reserved_bytes.argtypes = [P]
+    lib.mosaic_workspace_reserved_bytes.restype = ctypes.c_int64
+    lib.mosaic_workspace_destroy.argtypes = [P]
+    lib.mosaic_workspace_destroy.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -266,3 +278,81 @@ class Mosaic:
     @property
     def launches(self) -> int:
         return mosaic_launch_count(self.handle)
+
+
+# ------------------------------------------------------------------ VMM-backed output workspace
+
+def mosaic_workspace_create(device: int, reserve_bytes: int):
+    """Returns (status, workspace handle)."""
+    ws = ctypes.c_void_p()
+    st = load_library().mosaic_workspace_create(ctypes.byref(ws), int(device), int(reserve_bytes))
+    return st, ws
+
+
+def mosaic_workspace_bind(ws, nbytes: int):
+    """Returns (status, base address)."""
+    p = ctypes.c_void_p()
+    st = load_library().mosaic_workspace_bind(ws, int(nbytes), ctypes.byref(p))
+    return st, p.value
+
+
+def mosaic_workspace_trim(ws, keep_bytes: int) -> int:
+    return load_library().mosaic_workspace_trim(ws, int(keep_bytes))
+
+
+def mosaic_workspace_bound_bytes(ws) -> int:
+    return load_library().mosaic_workspace_bound_bytes(ws)
+
+
+def mosaic_workspace_reserved_bytes(ws) -> int:
+    return load_library().mosaic_workspace_reserved_bytes(ws)
+
+
+def mosaic_workspace_destroy(ws) -> int:
+    return load_library().mosaic_workspace_destroy(ws)
+
+
+class Workspace:
+    """Virtual range reserved once; physical pages bound only as far as `bind` asks."""
+
+    def __init__(self, reserve_bytes: int, device: int = 0):
+        st, ws = mosaic_workspace_create(device, reserve_bytes)
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        self.ws, self.device = ws, device
+
+    def bind(self, nbytes: int) -> int:
+        st, ptr = mosaic_workspace_bind(self.ws, nbytes)
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        return ptr
+
+    def tensor(self, shape, dtype):
+        """Bind enough pages for a contiguous tensor of `shape` and return a view of it."""
+        import torch
+
+        n = 1
+        for x in shape:
+            n *= int(x)
+        ptr = self.bind(n * torch.empty(0, dtype=dtype).element_size())
+        from .dlpack import device_view
+
+        return device_view(ptr, shape, dtype, self.device)
+
+    def trim(self, keep_bytes: int = 0):
+        st = mosaic_workspace_trim(self.ws, keep_bytes)
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+
+    @property
+    def bound_bytes(self) -> int:
+        return mosaic_workspace_bound_bytes(self.ws)
+
+    @property
+    def reserved_bytes(self) -> int:
+        return mosaic_workspace_reserved_bytes(self.ws)
+
+    def close(self):
+        if self.ws:
+            mosaic_workspace_destroy(self.ws)
+            self.ws = None

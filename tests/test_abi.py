@@ -32,7 +32,9 @@ def test_header_declares_the_api():
         "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
         "mosaic_launch_count", "mosaic_masked_logits", "mosaic_masked_logits_noalloc",
         "mosaic_masked_sample", "mosaic_masked_sample_workspace_bytes", "mosaic_min_chunk_rows",
-        "mosaic_set_wait_timeout"])
+        "mosaic_set_wait_timeout", "mosaic_workspace_bind", "mosaic_workspace_bound_bytes",
+        "mosaic_workspace_create", "mosaic_workspace_destroy", "mosaic_workspace_reserved_bytes",
+        "mosaic_workspace_trim"])
 
 
 def test_library_loads_and_exports_every_declared_symbol(lib_path):
@@ -126,3 +128,14 @@ def test_sample_workspace_bytes(lib_path):
     assert mosaic.mosaic_masked_sample_workspace_bytes(3686, 126464, 0) == 3 * 3686 * 496 * 4
     assert mosaic.mosaic_masked_sample_workspace_bytes(10000, 1000, 4096) == 3 * 4096 * 4 * 4
     assert mosaic.mosaic_masked_sample_workspace_bytes(-1, 10, 0) == -1
+
+
+def test_workspace_without_gpu_fails_cleanly(lib_path):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, ws = mosaic.mosaic_workspace_create(0, 1 << 30)
+    assert st == mosaic.MOSAIC_ERR_CUDA and not ws.value
+    assert mosaic.mosaic_workspace_bound_bytes(None) == -1
+    assert mosaic.mosaic_workspace_destroy(None) == mosaic.MOSAIC_OK
