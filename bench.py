@@ -258,8 +258,8 @@ def bench_reference(args):
 def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     """The same step end to end through the public call: every step copies its inputs (H, idx,
     CSR offsets and W) from pinned host memory to the device and reads all logits back to pinned
-    host memory. Copies run on their own streams so that member i's read-back overlaps member
-    i+1's compute; the timed region spans all of it."""
+    host memory. Uploads and read-backs run on their own streams and overlap compute and each
+    other (within and across steps); the timed region spans all of it."""
     import torch
 
     host_in, host_out = [], []
@@ -283,19 +283,28 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
 
+    # Ordering per member: its inputs may be overwritten once its compute has consumed them,
+    # its output buffer once its read-back is done. Nothing else is serialised, so uploads of
+    # step k+1 overlap read-backs of step k (opposite directions, separate copy engines).
+    consumed = [None] * len(calls)
+    read_back = [None] * len(calls)
+
     def e2e_step():
         Wd = None
-        s_in.wait_stream(stream)  # the previous step has consumed the device input buffers
-        for c, hi, di, ho, do in zip(calls, host_in, dev_in, host_out, dev_out):
+        for j, (c, hi, di, ho, do) in enumerate(zip(calls, host_in, dev_in, host_out, dev_out)):
             with torch.cuda.stream(s_in):
+                if consumed[j] is not None:
+                    s_in.wait_event(consumed[j])
                 for k2, v in hi.items():
                     di[k2].copy_(v, non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(s_in)
             stream.wait_event(ready)
+            if read_back[j] is not None:
+                stream.wait_event(read_back[j])
             Wd = di.get("W", Wd)
 
-            def on_chunk(ci, rb, rows, out, ho=ho):
+            def on_chunk(ci, rb, rows, out, ho=ho, c=c):
                 done = torch.cuda.Event()
                 done.record(stream)
                 s_out.wait_event(done)
@@ -308,9 +317,12 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
 
             mo.masked_logits(di["H"], di["idx"], Wd, di.get("so"), di.get("mo"), out=do,
                              chunk_rows=c["w"].chunk_rows, on_chunk=on_chunk, stream=stream)
-        fin = torch.cuda.Event()
-        fin.record(s_out)
-        stream.wait_event(fin)
+            consumed[j] = torch.cuda.Event()
+            consumed[j].record(stream)
+            read_back[j] = torch.cuda.Event()
+            read_back[j].record(s_out)
+        # W (member 0's input) is used by every member: not overwritten before the last is done
+        consumed[0] = consumed[-1]
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -321,8 +333,11 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     e1 = torch.cuda.Event(enable_timing=True)
     n_e2e = max(1, min(args.steps, args.e2e_steps))
     e0.record(stream)
+    s_in.wait_event(e0)
     for _ in range(n_e2e):
         e2e_step()
+    for ev in read_back:  # the timed region ends when the last logits are on the host
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1) / n_e2e
