@@ -349,6 +349,43 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
             "steps": n_e2e, "path": "pinned host -> Mosaic.masked_logits -> pinned host"}
 
 
+def bench_cublas_context(args, calls, tot_flops, stream):
+    """Context only (not a target, not this library): the same step done unfused by torch --
+    index_select of the masked rows into a gathered buffer, then a cuBLAS bf16 matmul with W^T
+    (flat index lists; CSR members use their resolved rows)."""
+    import torch
+
+    prepared = []
+    for c in calls:
+        m = c["mask"]
+        if m.seq_offsets is None:
+            rows = m.idx.long()
+        else:  # resolve the CSR batch once, outside the timed region
+            counts = (m.mask_offsets[1:] - m.mask_offsets[:-1]).long()
+            seq = torch.repeat_interleave(torch.arange(counts.numel(), device=counts.device), counts)
+            rows = m.seq_offsets.long()[seq] + m.idx.long()
+        prepared.append((c, rows))
+
+    def step():
+        for c, rows in prepared:
+            a = torch.index_select(c["H"], 0, rows)
+            torch.matmul(a, c["W"].t())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": tot_flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "what": "torch index_select + cuBLAS bf16 matmul (unfused, writes the gathered rows)"}
+
+
 def bench_cuda(args):
     import torch
 
@@ -454,6 +491,10 @@ def bench_cuda(args):
     if not args.no_e2e and args.mode == "logits":
         e2e = bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream)
 
+    cublas = None
+    if not args.no_cublas_context and args.mode == "logits":
+        cublas = bench_cublas_context(args, calls, tot_flops, stream)
+
     hbm, bf16, bf16_sus, peak_src = load_peaks()
     kernel_tflops = tot_flops * args.steps / (kernel_ms * 1e-3) / 1e12
     roof_time = max(tot_flops / (bf16 * 1e12), tot_bytes / (hbm * 1e9))
@@ -480,6 +521,7 @@ def bench_cuda(args):
             "hbm_peak_gbs": hbm,
         },
         "gpu_launches": launches,
+        "cublas_context": cublas,
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -510,6 +552,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas-context", action="store_true")
     ap.add_argument("--ref-step-s", type=float, default=15.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of the current kernel")

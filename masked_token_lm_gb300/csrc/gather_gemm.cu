@@ -9,12 +9,12 @@
 // buffer is ever written. The pages' kernel targeted RTX 3090 / A100; this one is designed for
 // Blackwell instead.
 //
-// Roles (per CTA, 352 threads):
-//   warps 6..9  A gather: each of the 128 threads resolves 8 of the tile's mask indices to
+// Roles (per CTA, 480 threads):
+//   warps 6..13 A gather: each of the 256 threads resolves 4 of the tile's mask indices to
 //               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
-//               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
+//               piece of each of its 4 rows with cp.async into the 128-byte-swizzled A stage of
 //               a STAGES-deep shared-memory ring (8 threads cover one 128-byte row segment).
-//   warp 10     relay: when a stage's gathered rows have landed, fences them into the async
+//   warp 14     relay: when a stage's gathered rows have landed, fences them into the async
 //               proxy and reports the stage to the (leader's) full barrier.
 //   warp 0      W stream: one thread issues a 2-D TMA load of the W tile per K block.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
@@ -65,10 +65,11 @@ constexpr int TMEM_COLS = 2 * BN;     // two accumulators
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
 constexpr int A_WARP0 = 6;
-constexpr int A_WARPS = 4;
+constexpr int A_WARPS = 8;
 constexpr int A_THREADS = 32 * A_WARPS;
-constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 10
-constexpr int NUM_THREADS = (RELAY_WARP + 1) * 32;  // 352
+constexpr int A_ROWS = BM * 8 / A_THREADS;       // rows per gather thread (8 threads per row)
+constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 14
+constexpr int NUM_THREADS = (RELAY_WARP + 1) * 32;  // 480
 constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
 
 template <bool PAIR>
@@ -299,66 +300,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= A_WARP0 && warp < RELAY_WARP) {
     // ---------------------------------------------------------------- A gather (cp.async)
-    const int at = threadIdx.x - A_WARP0 * 32;  // 0..127
-    const int chunk = at & 7;                   // 16-byte piece of a 128-byte row segment
-    const int row0 = at >> 3;                   // this thread's rows: row0 + 16 j, j = 0..7
-    const uint64_t pol_a = policy_evict_last(); // gathered rows are re-read by every N tile
+    // The gather warps' instruction stream is on the critical path (they issue every copy of
+    // the gathered rows), so the per-K-block work is kept to the copies themselves: addresses
+    // advance by a constant, destinations and byte counts are fixed per tile.
+    const int at = threadIdx.x - A_WARP0 * 32;    // 0 .. A_THREADS-1
+    const int chunk = at & 7;                     // 16-byte piece of a 128-byte row segment
+    const int row0 = at >> 3;                     // rows row0 + (A_THREADS / 8) * j
+    constexpr int ROW_STEP = A_THREADS / 8;
+    const uint64_t pol_a = policy_evict_last();   // gathered rows are re-read by every N tile
     const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
     const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
-    int64_t it = 0;  // K blocks issued by this warp across all of its tiles
+    const int k_full = p.d / BK;                  // K blocks with every piece inside d
+    const bool tail_in = chunk * 8 < p.d % BK;    // this piece in the partial last K block
+    uint32_t dst_off[A_ROWS];                     // 128-byte swizzle: piece ^ (row % 8)
+#pragma unroll
+    for (int j = 0; j < A_ROWS; ++j) {
+      const int r = row0 + ROW_STEP * j;
+      dst_off[j] = r * 128 + ((chunk ^ (r & 7)) << 4);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
     bool alive = true;
     // Index staging, part 2: the mask indices of a tile are loaded one tile ahead (they land
     // while the previous tile's K loop runs) and resolved to rows at the tile's start.
-    int32_t vnext[8];
-    auto load_idx = [&](int u, int32_t (&v)[8]) {
+    int32_t vnext[A_ROWS];
+    auto load_idx = [&](int u, int32_t (&v)[A_ROWS]) {
       const TileCoord t = unit_coord(u, rank, p);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = t.m * BM + row0 + 16 * j;
+      for (int j = 0; j < A_ROWS; ++j) {
+        const int r = t.m * BM + row0 + ROW_STEP * j;
         v[j] = r < p.rows ? __ldg(p.idx + p.row_begin + r) : 0;
       }
     };
     if (unit0 < num_units) load_idx(unit0, vnext);
     for (int u = unit0; u < num_units && alive; u += unit_stride) {
       const TileCoord tc = unit_coord(u, rank, p);
-      int32_t v[8];
+      int32_t v[A_ROWS];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = vnext[j];
+      for (int j = 0; j < A_ROWS; ++j) v[j] = vnext[j];
       if (u + unit_stride < num_units) load_idx(u + unit_stride, vnext);
-      // Rows past the chunk and rows with a bad index are zero-filled (src size 0: no read).
-      const char* src[8];
-      uint32_t valid = 0;
+      // Rows past the chunk and rows with a bad index are zero-filled: 0 source bytes (no read)
+      // from row 0 of H, an address that stays inside H for every full K block.
+      const char* src[A_ROWS];
+      uint32_t bytes[A_ROWS];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int r = tc.m * BM + row0 + 16 * j;
+      for (int j = 0; j < A_ROWS; ++j) {
+        const int r = tc.m * BM + row0 + ROW_STEP * j;
         bool ok = false;
         int32_t row = 0;
         if (r < p.rows) row = resolve_row(p, offs, p.row_begin + r, v[j], ok);
         src[j] = hbase + static_cast<int64_t>(row) * row_bytes;
-        valid |= (ok ? 1u : 0u) << j;
+        bytes[j] = ok ? 16u : 0u;
       }
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const int stage = static_cast<int>(it % STAGES);
-        const uint32_t phase = static_cast<uint32_t>((it / STAGES) & 1);
         int go = 1;
         if (lane == 0) go = wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p) ? 1 : 0;
         go = __shfl_sync(0xffffffffu, go, 0);
         if (!go) { alive = false; break; }
-        const bool k_in = kb * BK + chunk * 8 < p.d;  // d % 8 == 0: pieces are all in or out
         const uint32_t a_stage = sm.a(stage);
+        if (kb < k_full) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = row0 + 16 * j;
-          const uint32_t dst = a_stage + r * 128 + ((chunk ^ (r & 7)) << 4);
-          const bool live = k_in && ((valid >> j) & 1u);
-          // a zero-filling copy still names an address: keep it at the start of H
-          cp_async_16(dst, live ? src[j] + static_cast<int64_t>(kb) * (BK * 2) : hbase,
-                      live ? 16u : 0u, pol_a);
+          for (int j = 0; j < A_ROWS; ++j) cp_async_16(a_stage + dst_off[j], src[j], bytes[j], pol_a);
+        } else {  // partial last K block: pieces past d are zero-filled, named at the start of H
+#pragma unroll
+          for (int j = 0; j < A_ROWS; ++j)
+            cp_async_16(a_stage + dst_off[j], tail_in ? src[j] : hbase, tail_in ? bytes[j] : 0u, pol_a);
         }
+#pragma unroll
+        for (int j = 0; j < A_ROWS; ++j) src[j] += BK * 2;
         // Publish without waiting: the arrive on afull happens when these copies have landed;
         // the relay then fences them into the async proxy for the tensor cores.
         cp_async_arrive_noinc(sm.afull(stage));
-        ++it;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     cp_async_wait<0>();

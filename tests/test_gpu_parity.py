@@ -277,3 +277,47 @@ def test_min_chunk_rows_drives_a_chunked_call_within_budget(mo):
     full = run(mo, H, idx, W, torch.bfloat16)
     chunked = run(mo, H, idx, W, torch.bfloat16, chunk_rows=cr)
     assert torch.equal(full.view(torch.int16), chunked.view(torch.int16))
+
+
+@pytest.mark.parametrize("L,d,V,M,dt", [
+    (1, 8, 8, 1, torch.float32),        # smallest shape: one row, one 16-byte K piece, 8 columns
+    (50, 8, 8, 300, torch.float32),     # K far below one block, CTA pairs, duplicates
+    (512, 8192, 1024, 200, torch.bfloat16),  # 128 K blocks
+    (64, 24, 264, 130, torch.float32),  # K tail only (24 = 3 pieces), N tail of 8 columns
+])
+def test_extreme_shapes(mo, L, d, V, M, dt):
+    H, W = rand_inputs(L, d, V, seed=L * 7 + d + V)
+    g = torch.Generator().manual_seed(M)
+    idx = torch.randint(0, L, (M,), generator=g, dtype=torch.int32)
+    out = run(mo, H, idx.to(DEV), W, dt)
+    ref = orc.masked_logits(bits(H), idx.numpy(), bits(W))
+    assert_close(out, ref, dt, f"L={L} d={d} V={V} M={M}")
+
+
+def test_all_positions_masked_equals_the_full_gemm(mo):
+    L, d, V = 700, 256, 1288
+    H, W = rand_inputs(L, d, V, seed=91)
+    out = run(mo, H, torch.arange(L, dtype=torch.int32, device=DEV), W, torch.float32)
+    assert_close(out, orc.full_logits(bits(H), bits(W)), torch.float32, "all masked")
+
+
+def test_csr_duplicates_and_unsorted_local_indices(mo):
+    so = np.array([0, 100, 180, 400], np.int32)
+    moff = np.array([0, 5, 5, 12], np.int32)
+    idx = np.array([99, 3, 3, 50, 0, 219, 0, 7, 7, 100, 219, 1], np.int32)
+    d, V = 96, 776
+    H, W = rand_inputs(400, d, V, seed=93)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = run(mo, H, t(idx), W, torch.float32, t(so), t(moff))
+    ref = orc.masked_logits(bits(H), idx, bits(W), so, moff)
+    assert_close(out, ref, torch.float32, "csr duplicates")
+    assert torch.equal(out[1], out[2]) and torch.equal(out[5], out[10])
+
+
+def test_fp32_output_chunked_pairs_bitwise(mo):
+    L, d, V, M = 1500, 384, 2056, 700
+    H, W = rand_inputs(L, d, V, seed=95)
+    idx = wl.uniform_positions(L, M, seed=96).to(DEV)
+    full = run(mo, H, idx, W, torch.float32)
+    for cr in (129, 256, 500):
+        assert torch.equal(full, run(mo, H, idx, W, torch.float32, chunk_rows=cr))
