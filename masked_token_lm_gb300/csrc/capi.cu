@@ -299,9 +299,7 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     p.group_u = pick_group_u(p.m_units, cm, d);
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
-    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
-    const int64_t clusters = h->max_clusters[f32 ? 1 : 0][pair ? 1 : 0];
-    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
+    const int grid = mosaic::gather_gemm_schedule(p, h->max_clusters[f32 ? 1 : 0][pair ? 1 : 0]);
     e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     ++h->launches;
@@ -402,9 +400,7 @@ mosaic_status mosaic_masked_sample(mosaic_handle* h, const void* hidden, int64_t
     p.part_sum = part_sum;
     p.part_arg = part_arg;
     p.part_ld = static_cast<int32_t>(ld);
-    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
-    const int64_t clusters = h->max_clusters_sample[pair ? 1 : 0];
-    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
+    const int grid = mosaic::gather_gemm_schedule(p, h->max_clusters_sample[pair ? 1 : 0]);
     e = mosaic::gather_gemm_launch_sample(tm_w, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM (sampling) launch");
     e = mosaic::sample_reduce_launch(p, token, confidence, stream);
@@ -558,9 +554,7 @@ mosaic_status mosaic_masked_logits_noalloc(const void* hidden, int64_t L_tot, in
     p.group_u = pick_group_u(p.m_units, cm, d);
     p.status = nd->status + c;  // this chunk's word of the fixed array
     p.timeout_ns = 2000000000ull;
-    const int64_t units = static_cast<int64_t>(p.m_units) * p.n_tiles;
-    const int64_t clusters = nd->max_clusters[f32 ? 1 : 0][pair ? 1 : 0];
-    const int grid = static_cast<int>((units < clusters ? units : clusters) * cm);
+    const int grid = mosaic::gather_gemm_schedule(p, nd->max_clusters[f32 ? 1 : 0][pair ? 1 : 0]);
     e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     if (cb) cb(c, rb, rows, out, user);

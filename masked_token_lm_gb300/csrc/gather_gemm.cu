@@ -55,13 +55,15 @@ namespace mosaic {
 namespace {
 
 constexpr int BM = 128;  // rows of D per CTA
-constexpr int BN = 256;  // columns of D per tile
+constexpr int BN = 256;  // columns of one accumulator slot (one column panel)
 constexpr int BK = 64;   // 64 bf16 = 128 B = one swizzle row
 constexpr int UMMA_K = 16;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
 constexpr int EPI_BUF = BM * 128;     // 128 rows x 128 B
 constexpr int EPI_BUFS = 2;
-constexpr int TMEM_COLS = 2 * BN;     // two accumulators
+constexpr int TMEM_COLS = 2 * BN;     // two accumulator slots
+constexpr int STAGES = 4;
+constexpr int B_STAGE = 2 * 128 * BK * 2;  // 32 KiB of W rows per stage (both forms)
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_THREADS = 128;
 constexpr int A_WARP0 = 6;
@@ -74,9 +76,12 @@ constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1
 
 template <bool PAIR>
 struct Cfg {
-  static constexpr int STAGES = PAIR ? 6 : 4;
-  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // W rows per CTA per tile
-  static constexpr int B_STAGE = B_ROWS * BK * 2;    // 16 or 32 KiB
+  // Panels per unit: a pair computes 256 x 512 (two N = 256 MMAs per K step, one per TMEM slot);
+  // a single CTA computes 128 x 256, its two slots double-buffering successive tiles.
+  static constexpr int NSUB = PAIR ? 2 : 1;
+  static constexpr int B_BOX_ROWS = PAIR ? BN / 2 : BN;  // W rows per CTA per panel (one TMA box)
+  static constexpr int B_BOX = B_BOX_ROWS * BK * 2;      // 16 or 32 KiB
+  static_assert(NSUB * B_BOX == B_STAGE, "stage layout");
   static constexpr int SMEM_A_OFF = 0;
   static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE;
   static constexpr int SMEM_EPI_OFF = SMEM_B_OFF + STAGES * B_STAGE;
@@ -94,7 +99,10 @@ struct Cfg {
   static constexpr int FULL_COUNT = 2;
   static constexpr int TEMPTY_COUNT = PAIR ? 2 : 1;
   static constexpr int SIGNAL_BYTES = 16;
-  static constexpr uint32_t W_TX = (PAIR ? 2 : 1) * B_STAGE + (PAIR ? SIGNAL_BYTES : 0);
+  // Bytes the (leader's) full barrier expects per stage of a unit with nsub panels.
+  static __device__ __forceinline__ uint32_t w_tx(int nsub) {
+    return PAIR ? static_cast<uint32_t>(nsub * 2 * B_BOX + SIGNAL_BYTES) : B_BOX;
+  }
   static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -104,15 +112,18 @@ struct Smem {
   using C = Cfg<PAIR>;
   uint8_t* base;
   __device__ uint32_t a(int s) const { return smem_u32(base + C::SMEM_A_OFF + s * A_STAGE); }
-  __device__ uint32_t b(int s) const { return smem_u32(base + C::SMEM_B_OFF + s * C::B_STAGE); }
+  // W rows of panel j (0 .. NSUB-1) of stage s
+  __device__ uint32_t b(int s, int j = 0) const {
+    return smem_u32(base + C::SMEM_B_OFF + s * B_STAGE + j * C::B_BOX);
+  }
   __device__ uint32_t epi(int j) const { return smem_u32(base + C::SMEM_EPI_OFF + j * EPI_BUF); }
   __device__ uint32_t bar(int i) const { return smem_u32(base + C::SMEM_BAR_OFF + i * 8); }
   __device__ uint32_t full(int s) const { return bar(s); }
-  __device__ uint32_t empty(int s) const { return bar(C::STAGES + s); }
-  __device__ uint32_t afull(int s) const { return bar(2 * C::STAGES + s); }
-  __device__ uint32_t tfull(int j) const { return bar(3 * C::STAGES + j); }
-  __device__ uint32_t tempty(int j) const { return bar(3 * C::STAGES + 2 + j); }
-  __device__ uint32_t drain() const { return bar(3 * C::STAGES + 4); }
+  __device__ uint32_t empty(int s) const { return bar(STAGES + s); }
+  __device__ uint32_t afull(int s) const { return bar(2 * STAGES + s); }
+  __device__ uint32_t tfull(int j) const { return bar(3 * STAGES + j); }
+  __device__ uint32_t tempty(int j) const { return bar(3 * STAGES + 2 + j); }
+  __device__ uint32_t drain() const { return bar(3 * STAGES + 4); }
   __device__ uint32_t* tmem_slot() const {
     return reinterpret_cast<uint32_t*>(base + C::SMEM_MISC_OFF);
   }
@@ -193,11 +204,11 @@ struct TileCoord {
   int m, n;
 };
 
-// Work unit u = (cluster_m consecutive M tiles, one N panel). Units are rastered in groups of
-// group_u M units: N panels outer, M units inner. CTA `rank` of the pair takes M tile
-// mu * cluster_m + rank of the unit.
+// Whole unit u = (cluster_m consecutive M tiles, one unit column of n_sub panels). Units are
+// rastered in groups of group_u M units: unit columns outer, M units inner. CTA `rank` of the
+// pair takes M tile mu * cluster_m + rank of the unit; c.n is the unit column.
 __device__ __forceinline__ TileCoord unit_coord(int u, int rank, const GatherGemmParams& p) {
-  const int group_units = p.group_u * p.n_tiles;
+  const int group_units = p.group_u * p.n_wide;
   const int g = u / group_units;
   const int rem = u - g * group_units;
   const int mu_first = g * p.group_u;
@@ -208,13 +219,36 @@ __device__ __forceinline__ TileCoord unit_coord(int u, int rank, const GatherGem
   return c;
 }
 
+// What unit u of the schedule computes: M tile m, panels panel0 .. panel0 + nsub - 1. Units at
+// or past units_full are the halves of a split unit (one panel each). nsub = 0 for the empty
+// half of a unit column that has a single panel (odd n_tiles): every role skips it.
+struct Unit {
+  int m, panel0, nsub;
+};
+
+template <bool PAIR>
+__device__ __forceinline__ Unit unit_of(int u, int rank, const GatherGemmParams& p) {
+  int base = u, half = 0;
+  const bool split = u >= p.units_full;
+  if (split) {
+    const int h = u - p.units_full;
+    base = p.units_full + (h >> 1);
+    half = h & 1;
+  }
+  const TileCoord c = unit_coord(base, rank, p);
+  Unit t;
+  t.m = c.m;
+  t.panel0 = c.n * Cfg<PAIR>::NSUB + half;
+  t.nsub = min(split ? 1 : Cfg<PAIR>::NSUB, max(p.n_tiles - t.panel0, 0));
+  return t;
+}
+
 template <bool OUT_F32, bool PAIR, bool SAMPLE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_out,
                        const GatherGemmParams p) {
   using C = Cfg<PAIR>;
-  constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   Smem<PAIR> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -225,7 +259,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
   const int unit0 = static_cast<int>(blockIdx.x) / p.cluster_m;
   const int unit_stride = static_cast<int>(gridDim.x) / p.cluster_m;
-  const int num_units = p.m_units * p.n_tiles;
+  const int num_units = p.units_total;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -278,19 +312,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int u = unit0; u < num_units; u += unit_stride) {
-        const TileCoord tc = unit_coord(u, rank, p);
+        const Unit t = unit_of<PAIR>(u, rank, p);
+        if (t.nsub == 0) continue;
         bool alive = true;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
-          const int y = tc.n * BN + rank * C::B_ROWS;  // this CTA's half of the W tile
           if constexpr (PAIR) {
-            // The leader expects both halves; each CTA's load lands in its own shared memory
+            // Per panel, this CTA loads its 128-row half of the panel's 256 W rows. The leader
+            // expects the halves of both CTAs; each load lands in its own CTA's shared memory
             // and reports its bytes to the leader's barrier.
-            if (leader) mbar_arrive_expect_tx(sm.full(stage), C::W_TX);
-            tma_load_2d_pair(sm.b(stage), &tm_w, kb * BK, y, full_c(stage), pol_w);
+            if (leader) mbar_arrive_expect_tx(sm.full(stage), C::w_tx(t.nsub));
+            for (int j = 0; j < t.nsub; ++j)
+              tma_load_2d_pair(sm.b(stage, j), &tm_w, kb * BK,
+                               (t.panel0 + j) * BN + rank * C::B_BOX_ROWS, full_c(stage), pol_w);
           } else {
-            mbar_arrive_expect_tx(sm.full(stage), C::W_TX);
-            tma_load_2d(sm.b(stage), &tm_w, kb * BK, y, sm.full(stage), pol_w);
+            mbar_arrive_expect_tx(sm.full(stage), C::w_tx(1));
+            tma_load_2d(sm.b(stage), &tm_w, kb * BK, t.panel0 * BN, sm.full(stage), pol_w);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -325,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // while the previous tile's K loop runs) and resolved to rows at the tile's start.
     int32_t vnext[A_ROWS];
     auto load_idx = [&](int u, int32_t (&v)[A_ROWS]) {
-      const TileCoord t = unit_coord(u, rank, p);
+      const Unit t = unit_of<PAIR>(u, rank, p);
 #pragma unroll
       for (int j = 0; j < A_ROWS; ++j) {
         const int r = t.m * BM + row0 + ROW_STEP * j;
@@ -334,11 +371,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     if (unit0 < num_units) load_idx(unit0, vnext);
     for (int u = unit0; u < num_units && alive; u += unit_stride) {
-      const TileCoord tc = unit_coord(u, rank, p);
+      const Unit tc = unit_of<PAIR>(u, rank, p);
       int32_t v[A_ROWS];
 #pragma unroll
       for (int j = 0; j < A_ROWS; ++j) v[j] = vnext[j];
       if (u + unit_stride < num_units) load_idx(u + unit_stride, vnext);
+      if (tc.nsub == 0) continue;
       // Rows past the chunk and rows with a bad index are zero-filled: 0 source bytes (no read)
       // from row 0 of H, an address that stays inside H for every full K block.
       const char* src[A_ROWS];
@@ -389,6 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool alive = true;
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
+        if (unit_of<PAIR>(u, rank, p).nsub == 0) continue;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
           fence_proxy_async_smem();
@@ -404,31 +443,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      uint32_t tphase = 0;  // bit j: parity of the current use of accumulator slot j
+      int slot_next = 0;    // single CTA: tiles alternate between the two slots
       bool alive = true;
       bool issued_any = false;
+      // The 4 MMAs of one K block of panel j (W rows b(st, j)) into accumulator slot `slot`.
+      auto mma_kblock = [&](int st, int kb, int slot, int j) {
+        const uint64_t a0 = smem_desc_sw128(sm.a(st));
+        const uint64_t b0 = smem_desc_sw128(sm.b(st, j));
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k) {
+          // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
+          tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+        }
+      };
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
-        if (!wait_phase<PAIR>(sm.tempty(acc), acc_phase ^ 1u, sm, p)) { alive = false; break; }
+        const Unit t = unit_of<PAIR>(u, rank, p);
+        if (t.nsub == 0) continue;
+        const int s0 = PAIR ? 0 : slot_next;
+        if (!PAIR) slot_next ^= 1;
+        if (!wait_phase<PAIR>(sm.tempty(s0), ((tphase >> s0) & 1u) ^ 1u, sm, p)) { alive = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        // Two panels (pair): slot 1 may still be draining the previous unit's second panel. The
+        // slot-0 MMAs run ahead meanwhile, holding up to STAGES - 1 stages whose slot-1 MMAs are
+        // issued (oldest first) as soon as the slot is free.
+        const uint32_t s1_parity = ((tphase >> 1) & 1u) ^ 1u;
+        bool s1_free = t.nsub < 2;
+        int held = 0;
+        auto flush_held = [&](int kb_end) {
+          int hs = stage - held;
+          if (hs < 0) hs += STAGES;
+          for (int i = 0; i < held; ++i) {
+            mma_kblock(hs, kb_end - held + i, 1, 1);
+            tc_commit<PAIR>(sm.empty(hs));  // frees the stage once these MMAs have read it
+            if (++hs == STAGES) hs = 0;
+          }
+          held = 0;
+        };
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
           tc_fence_after();
-          const uint64_t a0 = smem_desc_sw128(sm.a(stage));
-          const uint64_t b0 = smem_desc_sw128(sm.b(stage));
-#pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
-            tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
-          }
-          tc_commit<PAIR>(sm.empty(stage));  // frees the stage once these MMAs have read it
+          mma_kblock(stage, kb, s0, 0);
           issued_any = true;
+          if (!s1_free) {
+            if (held < STAGES - 1 && !mbar_test_wait_cluster(sm.tempty(1), s1_parity)) {
+              ++held;
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+              continue;
+            }
+            if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
+            tc_fence_after();
+            s1_free = true;
+            flush_held(kb);
+          }
+          if (t.nsub == 2) mma_kblock(stage, kb, 1, 1);
+          tc_commit<PAIR>(sm.empty(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!alive) break;
-        tc_commit<PAIR>(sm.tfull(acc));  // accumulator complete
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        tc_commit<PAIR>(sm.tfull(s0));  // slot s0 complete
+        if (t.nsub == 2) {
+          if (!s1_free) {  // fewer K blocks than the stages the slot-0 MMAs may run ahead
+            if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
+            tc_fence_after();
+            flush_held(p.k_blocks);
+          }
+          tc_commit<PAIR>(sm.tfull(1));
+        }
+        tphase ^= (1u << s0) | (t.nsub == 2 ? 2u : 0u);
       }
       if (issued_any) {
         // Completes when every MMA issued above (and the arrives it triggers) has finished.
@@ -445,108 +528,118 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     constexpr int COLS_PER_CHUNK = OUT_F32 ? 32 : 64;  // 128 B of output per row
     constexpr int CHUNKS = BN / COLS_PER_CHUNK;
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    uint32_t tphase = 0;  // bit j: parity of the current use of accumulator slot j
+    int slot_next = 0;    // single CTA: tiles alternate between the two slots
     int buf = 0;
-    for (int u = unit0; u < num_units; u += unit_stride) {
-      const TileCoord tc = unit_coord(u, rank, p);
-      if (et == 0) *sm.epi_go() = wait_phase<false>(sm.tfull(acc), acc_phase, sm, p) ? 1 : 0;
-      named_bar_sync(1, EPI_THREADS);
-      if (!*sm.epi_go()) break;
-      tc_fence_after();
+    bool go = true;
+    for (int u = unit0; u < num_units && go; u += unit_stride) {
+      const Unit tc = unit_of<PAIR>(u, rank, p);
+      if (tc.nsub == 0) continue;
+      // The row this thread stores is the same for every panel of the unit.
       const int r = tc.m * BM + row_in_tile;
       bool ok = true;
       if (r < p.rows) {
         resolve_row(p, offs, p.row_begin + r, __ldg(p.idx + p.row_begin + r), ok);
         if (!ok) atomicOr(p.status, MOSAIC_STATUS_INDEX);
       }
-      const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(acc * BN);
-      const int n0 = tc.n * BN;
-      if constexpr (SAMPLE) {
-        // Sampling epilogue: this row's running max, first argmax and sum of exp(x - max) over
-        // the tile's valid columns (fp32 logits straight from TMEM), merged chunk by chunk.
-        float m = -INFINITY, s = 0.0f;
-        int a = 0;
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(t_acc + c * 32, v);
-          tmem_wait_ld();
-          const int col0 = n0 + c * 32;
-          float cm = -INFINITY;
-          int ca = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = __uint_as_float(v[j]);
-            if (col0 + j < p.V && x > cm) { cm = x; ca = col0 + j; }
-          }
-          if (cm > m) { s *= __expf(m - cm); m = cm; a = ca; }
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (col0 + j < p.V) s += __expf(__uint_as_float(v[j]) - m);
-        }
-        tc_fence_before();  // this thread's TMEM reads are done
+      for (int jp = 0; jp < tc.nsub; ++jp) {
+        // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
+        const int slot = PAIR ? jp : slot_next;
+        if (!PAIR) slot_next ^= 1;
+        if (et == 0)
+          *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
         named_bar_sync(1, EPI_THREADS);
-        if (et == 0) {
-          if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
-        }
-        if (r < p.rows && tc.m < p.m_tiles) {
-          const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.n;
-          p.part_max[o] = m;
-          p.part_sum[o] = s;
-          p.part_arg[o] = ok ? a : -1;
-        }
-      } else {
-        for (int c = 0; c < CHUNKS; ++c) {
-          uint32_t packed[32];
-          if constexpr (OUT_F32) {
-            tmem_ld_32x32b_x32(t_acc + c * 32, packed);
+        if (!*sm.epi_go()) { go = false; break; }
+        tc_fence_after();
+        tphase ^= 1u << slot;
+        const int panel = tc.panel0 + jp;
+        const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN);
+        const int n0 = panel * BN;
+        if constexpr (SAMPLE) {
+          // Sampling epilogue: this row's running max, first argmax and sum of exp(x - max) over
+          // the tile's valid columns (fp32 logits straight from TMEM), merged chunk by chunk.
+          float m = -INFINITY, s = 0.0f;
+          int a = 0;
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_acc + c * 32, v);
             tmem_wait_ld();
-            if (!ok) {
+            const int col0 = n0 + c * 32;
+            float cm = -INFINITY;
+            int ca = 0;
   #pragma unroll
-              for (int j = 0; j < 32; ++j) packed[j] = 0u;
+            for (int j = 0; j < 32; ++j) {
+              const float x = __uint_as_float(v[j]);
+              if (col0 + j < p.V && x > cm) { cm = x; ca = col0 + j; }
             }
-          } else {
-            uint32_t v0[32], v1[32];
-            tmem_ld_32x32b_x32(t_acc + c * 64, v0);
-            tmem_ld_32x32b_x32(t_acc + c * 64 + 32, v1);
-            tmem_wait_ld();
+            if (cm > m) { s *= __expf(m - cm); m = cm; a = ca; }
   #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              packed[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
-              packed[16 + j] =
-                  pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
-            }
-            if (!ok) {
-  #pragma unroll
-              for (int j = 0; j < 32; ++j) packed[j] = 0u;
-            }
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.V) s += __expf(__uint_as_float(v[j]) - m);
           }
-          if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
-          // The staging buffer is free once the store issued from it two chunks ago has read it.
-          if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
-          named_bar_sync(1, EPI_THREADS);
-          if (c == CHUNKS - 1 && et == 0) {
-            // All columns of this accumulator are in registers: hand it back to the MMA issuer.
-            if (PAIR) mbar_arrive_cluster(tempty_c(acc)); else mbar_arrive(sm.tempty(acc));
-          }
-          const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
-          const int sw = row_in_tile & 7;
-  #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            st_shared_v4(dst + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                         packed[4 * j + 3]);
-          }
-          fence_proxy_async_smem();
+          tc_fence_before();  // this thread's TMEM reads are done
           named_bar_sync(1, EPI_THREADS);
           if (et == 0) {
-            const int x = n0 + c * COLS_PER_CHUNK;
-            if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
-            bulk_commit_group();
+            if (PAIR) mbar_arrive_cluster(tempty_c(slot)); else mbar_arrive(sm.tempty(slot));
           }
-          buf ^= 1;
+          if (r < p.rows && tc.m < p.m_tiles) {
+            const int64_t o = static_cast<int64_t>(r) * p.part_ld + panel;
+            p.part_max[o] = m;
+            p.part_sum[o] = s;
+            p.part_arg[o] = ok ? a : -1;
+          }
+        } else {
+          for (int c = 0; c < CHUNKS; ++c) {
+            uint32_t packed[32];
+            if constexpr (OUT_F32) {
+              tmem_ld_32x32b_x32(t_acc + c * 32, packed);
+              tmem_wait_ld();
+              if (!ok) {
+    #pragma unroll
+                for (int j = 0; j < 32; ++j) packed[j] = 0u;
+              }
+            } else {
+              uint32_t v0[32], v1[32];
+              tmem_ld_32x32b_x32(t_acc + c * 64, v0);
+              tmem_ld_32x32b_x32(t_acc + c * 64 + 32, v1);
+              tmem_wait_ld();
+    #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                packed[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+                packed[16 + j] =
+                    pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+              }
+              if (!ok) {
+    #pragma unroll
+                for (int j = 0; j < 32; ++j) packed[j] = 0u;
+              }
+            }
+            if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
+            // The staging buffer is free once the store issued from it two chunks ago has read it.
+            if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
+            named_bar_sync(1, EPI_THREADS);
+            if (c == CHUNKS - 1 && et == 0) {
+              // All columns of this accumulator are in registers: hand it back to the MMA issuer.
+              if (PAIR) mbar_arrive_cluster(tempty_c(slot)); else mbar_arrive(sm.tempty(slot));
+            }
+            const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
+            const int sw = row_in_tile & 7;
+    #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              st_shared_v4(dst + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                           packed[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, EPI_THREADS);
+            if (et == 0) {
+              const int x = n0 + c * COLS_PER_CHUNK;
+              if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
+              bulk_commit_group();
+            }
+            buf ^= 1;
+          }
         }
-      }
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }  // panels of the unit
     }
     if (et == 0) bulk_wait_group_all();
   }
@@ -642,7 +735,29 @@ int gather_gemm_block_m() { return BM; }
 int gather_gemm_block_n() { return BN; }
 int gather_gemm_block_k() { return BK; }
 int gather_gemm_epi_cols(bool out_f32) { return out_f32 ? 32 : 64; }
-int gather_gemm_w_box_rows(bool pair) { return pair ? Cfg<true>::B_ROWS : Cfg<false>::B_ROWS; }
+int gather_gemm_w_box_rows(bool pair) {
+  return pair ? Cfg<true>::B_BOX_ROWS : Cfg<false>::B_BOX_ROWS;
+}
+
+int gather_gemm_schedule(GatherGemmParams& p, int max_clusters) {
+  const int nsub = p.cluster_m == 2 ? Cfg<true>::NSUB : Cfg<false>::NSUB;
+  p.n_wide = (p.n_tiles + nsub - 1) / nsub;
+  const int64_t units = static_cast<int64_t>(p.m_units) * p.n_wide;
+  p.units_full = p.units_total = static_cast<int32_t>(units);
+  const int64_t P = max_clusters > 0 ? max_clusters : 1;
+  if (nsub > 1) {
+    // A last round that keeps at most half of the clusters busy is run as twice as many
+    // single-panel units instead, so that every cluster shares it.
+    const int64_t rounds = (units + P - 1) / P;
+    const int64_t last = units - (rounds - 1) * P;
+    if (units > 0 && 2 * last <= P) {
+      p.units_full = static_cast<int32_t>((rounds - 1) * P);
+      p.units_total = static_cast<int32_t>(p.units_full + 2 * last);
+    }
+  }
+  const int64_t clusters = p.units_total < P ? p.units_total : P;
+  return static_cast<int>(clusters * p.cluster_m);
+}
 
 cudaError_t gather_gemm_prepare_sample(bool pair, int* clusters) {
   return pair ? prepare_one<false, true, true>(clusters) : prepare_one<false, false, true>(clusters);

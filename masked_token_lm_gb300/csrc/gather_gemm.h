@@ -25,10 +25,18 @@ struct GatherGemmParams {
   int32_t V;
   int32_t d;
   int32_t k_blocks;             // ceil(d / BK)
-  int32_t m_tiles, n_tiles;     // ceil(rows / BM), ceil(V / BN)
+  int32_t m_tiles, n_tiles;     // ceil(rows / BM), ceil(V / BN): BN-wide column panels
   int32_t cluster_m;            // 2: a CTA pair computes 256-row tiles (cta_group::2); 1: single
   int32_t m_units;              // ceil(m_tiles / cluster_m)
   int32_t group_u;              // M units per raster group
+  // Work units (set by gather_gemm_schedule): a unit is one M unit times n_sub consecutive
+  // panels (n_sub = 2 for a pair, 1 for a single CTA); n_wide = ceil(n_tiles / n_sub) unit
+  // columns. Units [0, units_full) are whole; when the last round of the persistent schedule is
+  // at most half full, its units are split into two single-panel units each, numbered
+  // units_full .. units_total - 1.
+  int32_t n_wide;
+  int32_t units_full;
+  int32_t units_total;
   uint32_t* status;             // device status word
   uint64_t timeout_ns;          // bound on any single wait
   // Sampling epilogue only: per (row, N tile) partials at row * part_ld + n_tile.
@@ -43,6 +51,9 @@ int gather_gemm_block_n();
 int gather_gemm_block_k();
 int gather_gemm_epi_cols(bool out_f32);
 int gather_gemm_w_box_rows(bool pair);
+// Fills p.n_wide / units_full / units_total from p.m_units, p.n_tiles and p.cluster_m for a grid
+// of at most max_clusters clusters, and returns the grid size in CTAs.
+int gather_gemm_schedule(GatherGemmParams& p, int max_clusters);
 // Sets the kernel's shared-memory attribute and reports how many clusters fit at once.
 cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters);
 // Same for the sampling epilogue.
