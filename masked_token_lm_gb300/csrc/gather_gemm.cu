@@ -10,35 +10,41 @@
 // Blackwell instead.
 //
 // Roles (per CTA, 480 threads):
-//   warps 6..13 A gather: each of the 256 threads resolves 4 of the tile's mask indices to
+//   warps 10..13 A gather: each of the 128 threads resolves 8 of the tile's mask indices to
 //               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
-//               piece of each of its 4 rows with cp.async into the 128-byte-swizzled A stage of
-//               a STAGES-deep shared-memory ring (8 threads cover one 128-byte row segment).
+//               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
+//               a 4-deep shared-memory ring (8 threads cover one 128-byte row segment).
 //   warp 14     relay: when a stage's gathered rows have landed, fences them into the async
 //               proxy and reports the stage to the (leader's) full barrier.
-//   warp 0      W stream: one thread issues a 2-D TMA load of the W tile per K block.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
-//               accumulator (2 x 256 fp32 columns) and commits stage releases.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator, round to bf16 (or keep fp32), write
-//               128-byte-swizzled staging tiles and TMA-store them; rows past the chunk are
-//               clipped by the store's tensor map.
+//   warp 0      W stream: one thread issues the 2-D TMA loads of the W rows of each K block.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma into two 256-column TMEM accumulator
+//               slots and commits stage releases.
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant, each half of them taking 128
+//               columns of a slot: tcgen05.ld the accumulator into registers (rounded to bf16),
+//               hand the slot back, then write 128-byte-swizzled staging tiles and TMA-store
+//               them; rows past the chunk are clipped by the store's tensor map.
 //
-// PAIR = true (the normal case): two CTAs of a cluster form a pair that computes a 256 x 256
-// tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), issued by the leader CTA.
-// Each CTA gathers its own 128 A rows and loads its own 128-row half of the W tile, so every
-// SM takes in 32 KiB per K block instead of 48 KiB; per-SM ingress was the measured limit of
-// the single-CTA 128 x 256 form. The leader's stage barriers collect the whole pair: its W
-// expect_tx covers both halves (each CTA's cta_group::2 TMA load reports its bytes there), and
-// each CTA's relay reports its own gathered rows. Commits multicast to both CTAs. PAIR = false runs
-// 128 x 256 tiles on one CTA (problems with a single M tile).
+// PAIR = true (the normal case): two CTAs of a cluster form a pair that computes a 256 x 512
+// unit: per K step two tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), one per adjacent
+// 256-column panel, each into its own TMEM slot, issued by the leader CTA. Each CTA gathers its
+// own 128 A rows and loads its own 128-row half of each panel's W rows, so per K block an SM
+// takes in 16 KiB of gathered rows and 32 KiB of W for 2 x 2^22 FLOP: 48 bytes per tensor-core
+// cycle (a 256 x 256 unit needs 64 and measured ~81 % tensor-pipe busy against ~89 % for this).
+// The leader's stage barriers collect the whole pair: its W expect_tx covers the boxes of both
+// CTAs (each CTA's cta_group::2 TMA load reports its bytes there), and each CTA's relay reports
+// its own gathered rows. Commits multicast to both CTAs. The slots are drained one after the
+// other; the MMA issuer starts the next unit's slot-0 MMAs while slot 1 is still being read,
+// holding up to 3 stages whose slot-1 MMAs it issues once that slot is free. PAIR = false runs
+// 128 x 256 tiles on one CTA (problems with a single M tile), alternating the two slots.
 //
 // The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
 // 32 gather4 instructions a 128-row K block needs held the kernel to ~26 % of the tensor peak,
 // while the same bytes through the load/store units keep the tensor pipe fed.
 //
-// Tiles are walked by a static persistent schedule over units (one M tile per CTA of the pair,
-// one N panel): within a group of M units, N panels outer and M units inner, so each W panel is
-// fetched from HBM once per group while the gathered A rows of the group stay in L2.
+// Units are walked by a static persistent schedule (one M tile per CTA of the pair, one unit
+// column of panels): within a group of M units, unit columns outer and M units inner, so each W
+// panel is fetched from HBM once per group while the gathered A rows of the group stay in L2.
+// A last round that would keep at most half the clusters busy is split into single-panel units.
 //
 // Every wait is bounded (globaltimer); a wait that runs out records MOSAIC status bit 2, makes
 // all roles stop, lets in-flight copies and MMAs finish, frees TMEM and returns.
@@ -60,14 +66,14 @@ constexpr int BK = 64;   // 64 bf16 = 128 B = one swizzle row
 constexpr int UMMA_K = 16;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
 constexpr int EPI_BUF = BM * 128;     // 128 rows x 128 B
-constexpr int EPI_BUFS = 2;
+constexpr int EPI_BUFS = 2;           // one per epilogue half
 constexpr int TMEM_COLS = 2 * BN;     // two accumulator slots
 constexpr int STAGES = 4;
 constexpr int B_STAGE = 2 * 128 * BK * 2;  // 32 KiB of W rows per stage (both forms)
 constexpr int EPI_WARP0 = 2;
-constexpr int EPI_THREADS = 128;
-constexpr int A_WARP0 = 6;
-constexpr int A_WARPS = 8;
+constexpr int EPI_THREADS = 256;      // warps 2..9: two per TMEM lane quadrant
+constexpr int A_WARP0 = 10;
+constexpr int A_WARPS = 4;
 constexpr int A_THREADS = 32 * A_WARPS;
 constexpr int A_ROWS = BM * 8 / A_THREADS;       // rows per gather thread (8 threads per row)
 constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 14
@@ -522,16 +528,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int et = threadIdx.x - EPI_WARP0 * 32;   // 0..127
-    const int quad = warp & 3;                     // TMEM lane quadrant this warp may read
+    // Two warps per TMEM lane quadrant: warp w may read lanes 32 * (w % 4) .. + 31, and the
+    // warps of half h = 0 / 1 take columns h * 128 .. + 127 of the accumulator slot. Each half
+    // stages its output through its own 128-byte-swizzled buffer and TMA-stores it.
+    const int et = threadIdx.x - EPI_WARP0 * 32;   // 0 .. EPI_THREADS-1
+    const int half = et / (EPI_THREADS / 2);
+    const int gt = et % (EPI_THREADS / 2);         // thread within the half
+    const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    constexpr int COLS_PER_CHUNK = OUT_F32 ? 32 : 64;  // 128 B of output per row
-    constexpr int CHUNKS = BN / COLS_PER_CHUNK;
+    const uint32_t stage_buf = sm.epi(half);
+    const uint32_t bar_half = 2 + half;           // named barrier of this half's 128 threads
     uint32_t tphase = 0;  // bit j: parity of the current use of accumulator slot j
     int slot_next = 0;    // single CTA: tiles alternate between the two slots
-    int buf = 0;
     bool go = true;
+    // One 128-byte row segment of this thread's output row into the half's staging buffer, then
+    // one TMA store of the buffer (rows past the chunk are clipped by the tensor map).
+    auto stage_store = [&](const uint32_t (&w)[32], int x, int m_tile) {
+      if (gt == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
+      named_bar_sync(bar_half, EPI_THREADS / 2);
+      const uint32_t dst = stage_buf + row_in_tile * 128;
+      const int sw = row_in_tile & 7;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(dst + ((j ^ sw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      fence_proxy_async_smem();
+      named_bar_sync(bar_half, EPI_THREADS / 2);
+      if (gt == 0) {
+        if (x < p.V && m_tile < p.m_tiles) tma_store_2d(&tm_out, stage_buf, x, m_tile * BM);
+        bulk_commit_group();
+      }
+    };
+    // All TMEM reads of the slot are done in every epilogue thread: hand it back to the MMA issuer.
+    auto release_slot = [&](int slot) {
+      tc_fence_before();
+      named_bar_sync(1, EPI_THREADS);
+      if (et == 0) {
+        if (PAIR) mbar_arrive_cluster(tempty_c(slot)); else mbar_arrive(sm.tempty(slot));
+      }
+    };
     for (int u = unit0; u < num_units && go; u += unit_stride) {
       const Unit tc = unit_of<PAIR>(u, rank, p);
       if (tc.nsub == 0) continue;
@@ -540,7 +575,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       if (r < p.rows) {
         resolve_row(p, offs, p.row_begin + r, __ldg(p.idx + p.row_begin + r), ok);
-        if (!ok) atomicOr(p.status, MOSAIC_STATUS_INDEX);
+        if (!ok && half == 0) atomicOr(p.status, MOSAIC_STATUS_INDEX);
       }
       for (int jp = 0; jp < tc.nsub; ++jp) {
         // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
@@ -552,96 +587,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!*sm.epi_go()) { go = false; break; }
         tc_fence_after();
         tphase ^= 1u << slot;
-        const int panel = tc.panel0 + jp;
-        const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN);
-        const int n0 = panel * BN;
+        const int col_h = half * (BN / 2);  // first slot column of this half
+        const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
+        const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
         if constexpr (SAMPLE) {
           // Sampling epilogue: this row's running max, first argmax and sum of exp(x - max) over
-          // the tile's valid columns (fp32 logits straight from TMEM), merged chunk by chunk.
+          // the half's valid columns (fp32 logits straight from TMEM), merged chunk by chunk;
+          // then the two halves of the row are merged through shared memory.
           float m = -INFINITY, s = 0.0f;
           int a = 0;
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = 0; c < BN / 2 / 32; ++c) {
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_acc + c * 32, v);
             tmem_wait_ld();
             const int col0 = n0 + c * 32;
             float cm = -INFINITY;
             int ca = 0;
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float x = __uint_as_float(v[j]);
               if (col0 + j < p.V && x > cm) { cm = x; ca = col0 + j; }
             }
             if (cm > m) { s *= __expf(m - cm); m = cm; a = ca; }
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 32; ++j)
               if (col0 + j < p.V) s += __expf(__uint_as_float(v[j]) - m);
           }
-          tc_fence_before();  // this thread's TMEM reads are done
-          named_bar_sync(1, EPI_THREADS);
-          if (et == 0) {
-            if (PAIR) mbar_arrive_cluster(tempty_c(slot)); else mbar_arrive(sm.tempty(slot));
+          float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);
+          float* xs = xm + BM;
+          int* xa = reinterpret_cast<int*>(xs + BM);
+          if (half == 1) { xm[row_in_tile] = m; xs[row_in_tile] = s; xa[row_in_tile] = a; }
+          release_slot(slot);  // also orders the exchange above before the reads below
+          if (half == 0) {
+            const float m1 = xm[row_in_tile], s1 = xs[row_in_tile];
+            const int a1 = xa[row_in_tile];
+            // columns of half 0 come first: an equal maximum keeps half 0's index
+            if (m1 > m) { s = s * __expf(m - m1) + s1; m = m1; a = a1; }
+            else if (s1 > 0.0f) { s += s1 * __expf(m1 - m); }
+            if (r < p.rows && tc.m < p.m_tiles) {
+              const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
+              p.part_max[o] = m;
+              p.part_sum[o] = s;
+              p.part_arg[o] = ok ? a : -1;
+            }
           }
-          if (r < p.rows && tc.m < p.m_tiles) {
-            const int64_t o = static_cast<int64_t>(r) * p.part_ld + panel;
-            p.part_max[o] = m;
-            p.part_sum[o] = s;
-            p.part_arg[o] = ok ? a : -1;
+        } else if constexpr (OUT_F32) {
+          // fp32 out: 4 chunks of 32 columns (128 B per row), the slot released after the last load
+          for (int c = 0; c < BN / 2 / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(t_acc + c * 32, v);
+            tmem_wait_ld();
+            if (!ok) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0u;
+            }
+            if (c == BN / 2 / 32 - 1) release_slot(slot);
+            stage_store(v, n0 + c * 32, tc.m);
           }
         } else {
-          for (int c = 0; c < CHUNKS; ++c) {
-            uint32_t packed[32];
-            if constexpr (OUT_F32) {
-              tmem_ld_32x32b_x32(t_acc + c * 32, packed);
-              tmem_wait_ld();
-              if (!ok) {
-    #pragma unroll
-                for (int j = 0; j < 32; ++j) packed[j] = 0u;
-              }
-            } else {
-              uint32_t v0[32], v1[32];
-              tmem_ld_32x32b_x32(t_acc + c * 64, v0);
-              tmem_ld_32x32b_x32(t_acc + c * 64 + 32, v1);
-              tmem_wait_ld();
-    #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                packed[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
-                packed[16 + j] =
-                    pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
-              }
-              if (!ok) {
-    #pragma unroll
-                for (int j = 0; j < 32; ++j) packed[j] = 0u;
-              }
-            }
-            if (c == CHUNKS - 1) tc_fence_before();  // this thread's TMEM reads are done
-            // The staging buffer is free once the store issued from it two chunks ago has read it.
-            if (et == 0) bulk_wait_group_read<EPI_BUFS - 1>();
-            named_bar_sync(1, EPI_THREADS);
-            if (c == CHUNKS - 1 && et == 0) {
-              // All columns of this accumulator are in registers: hand it back to the MMA issuer.
-              if (PAIR) mbar_arrive_cluster(tempty_c(slot)); else mbar_arrive(sm.tempty(slot));
-            }
-            const uint32_t dst = sm.epi(buf) + row_in_tile * 128;
-            const int sw = row_in_tile & 7;
-    #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              st_shared_v4(dst + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                           packed[4 * j + 3]);
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, EPI_THREADS);
-            if (et == 0) {
-              const int x = n0 + c * COLS_PER_CHUNK;
-              if (x < p.V && tc.m < p.m_tiles) tma_store_2d(&tm_out, sm.epi(buf), x, tc.m * BM);
-              bulk_commit_group();
-            }
-            buf ^= 1;
+          // bf16 out: the half's 128 columns go to registers (rounded and packed) before any
+          // store, so the slot is handed back after 4 TMEM loads rather than after the stores.
+          uint32_t packed[2][32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(t_acc + q * 16, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              packed[q >> 2][(q & 3) * 8 + j] =
+                  pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
           }
+          release_slot(slot);
+          if (!ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) { packed[0][j] = 0u; packed[1][j] = 0u; }
+          }
+          stage_store(packed[0], n0, tc.m);
+          stage_store(packed[1], n0 + 64, tc.m);
         }
       }  // panels of the unit
     }
-    if (et == 0) bulk_wait_group_all();
+    if (gt == 0) bulk_wait_group_all();
   }
 
   tc_fence_before();
