@@ -82,8 +82,8 @@ bool is_device_ptr(const void* p, int device) {
   return a.type == cudaMemoryTypeManaged;
 }
 
-// 2-D row-major tensor [rows, cols] of `elt`-byte elements, box {box_cols, box_rows}, 128-byte
-// swizzle (box_cols * elt == 128), zero fill outside the tensor.
+// 2-D row-major tensor [rows, cols] of `elt`-byte elements, box {box_cols, box_rows}, swizzled
+// at the width of a box row (box_cols * elt: 64 or 128 bytes), zero fill outside the tensor.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* base,
                uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
   auto fn = encode_fn();
@@ -93,7 +93,8 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* b
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_cols * elt == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -62,7 +62,12 @@ namespace {
 
 constexpr int BM = 128;  // rows of D per CTA
 constexpr int BN = 256;  // columns of one accumulator slot (one column panel)
-constexpr int BK = 64;   // 64 bf16 = 128 B = one swizzle row
+// K block: 64 bf16 = 128-byte rows, stored with the 128-byte swizzle. (32 with the 64-byte
+// swizzle and 8 stages computes the same bits but measured 17-24 % slower on GB300: the per-stage
+// costs of the producers and the relay no longer fit in a 512-cycle K block.)
+constexpr int BK = 64;
+constexpr int ROW_BYTES = BK * 2;
+constexpr int PIECES = ROW_BYTES / 16;  // 16-byte pieces per row of a K block
 constexpr int UMMA_K = 16;
 constexpr int A_STAGE = BM * BK * 2;  // 16 KiB
 constexpr int EPI_BUF = BM * 128;     // 128 rows x 128 B
@@ -75,7 +80,7 @@ constexpr int EPI_THREADS = 256;      // warps 2..9: two per TMEM lane quadrant
 constexpr int A_WARP0 = 10;
 constexpr int A_WARPS = 4;
 constexpr int A_THREADS = 32 * A_WARPS;
-constexpr int A_ROWS = BM * 8 / A_THREADS;       // rows per gather thread (8 threads per row)
+constexpr int A_ROWS = BM * PIECES / A_THREADS;  // rows per gather thread (PIECES threads per row)
 constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 14
 constexpr int NUM_THREADS = (RELAY_WARP + 1) * 32;  // 480
 constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
@@ -347,19 +352,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the gathered rows), so the per-K-block work is kept to the copies themselves: addresses
     // advance by a constant, destinations and byte counts are fixed per tile.
     const int at = threadIdx.x - A_WARP0 * 32;    // 0 .. A_THREADS-1
-    const int chunk = at & 7;                     // 16-byte piece of a 128-byte row segment
-    const int row0 = at >> 3;                     // rows row0 + (A_THREADS / 8) * j
-    constexpr int ROW_STEP = A_THREADS / 8;
+    const int chunk = at % PIECES;                // 16-byte piece of a row segment
+    const int row0 = at / PIECES;                 // rows row0 + ROW_STEP * j
+    constexpr int ROW_STEP = A_THREADS / PIECES;
     const uint64_t pol_a = policy_evict_last();   // gathered rows are re-read by every N tile
     const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
     const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
     const int k_full = p.d / BK;                  // K blocks with every piece inside d
     const bool tail_in = chunk * 8 < p.d % BK;    // this piece in the partial last K block
-    uint32_t dst_off[A_ROWS];                     // 128-byte swizzle: piece ^ (row % 8)
+    // The swizzle of TMA and of the MMA descriptors: the piece index (address bits 4..) is
+    // XORed with address bits 7.. of the row start (64-byte rows: (row / 2) % 4; 128: row % 8).
+    uint32_t dst_off[A_ROWS];
 #pragma unroll
     for (int j = 0; j < A_ROWS; ++j) {
       const int r = row0 + ROW_STEP * j;
-      dst_off[j] = r * 128 + ((chunk ^ (r & 7)) << 4);
+      dst_off[j] = r * ROW_BYTES + ((chunk ^ ((r * ROW_BYTES >> 7) & (PIECES - 1))) << 4);
     }
     int stage = 0;
     uint32_t phase = 0;
@@ -455,8 +462,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool issued_any = false;
       // The 4 MMAs of one K block of panel j (W rows b(st, j)) into accumulator slot `slot`.
       auto mma_kblock = [&](int st, int kb, int slot, int j) {
-        const uint64_t a0 = smem_desc_sw128(sm.a(st));
-        const uint64_t b0 = smem_desc_sw128(sm.b(st, j));
+        const uint64_t a0 = smem_desc_kmajor<ROW_BYTES>(sm.a(st));
+        const uint64_t b0 = smem_desc_kmajor<ROW_BYTES>(sm.b(st, j));
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {

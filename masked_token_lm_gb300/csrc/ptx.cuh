@@ -316,15 +316,18 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major operand tile stored with the 128-byte swizzle
-// (rows of 128 B, 8-row groups 1024 B apart), as written by TMA with CU_TENSOR_MAP_SWIZZLE_128B.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are ROW_BYTES (64 or
+// 128) bytes wide and stored with the swizzle of that width, as TMA writes them with
+// CU_TENSOR_MAP_SWIZZLE_64B / _128B: 8-row groups ROW_BYTES * 8 bytes apart.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr) {
+  static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "swizzle width");
   uint64_t desc = 0;
-  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address, 16-B units
-  desc |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused, SW128 K-major)
-  desc |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: 8 rows x 128 B
-  desc |= static_cast<uint64_t>(1) << 46;                   // descriptor version (tcgen05)
-  desc |= static_cast<uint64_t>(2) << 61;                   // swizzle mode: 128 B
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);         // start address, 16-B units
+  desc |= static_cast<uint64_t>(1) << 16;                          // leading byte offset (unused)
+  desc |= static_cast<uint64_t>((ROW_BYTES * 8) >> 4) << 32;       // stride byte offset
+  desc |= static_cast<uint64_t>(1) << 46;                          // descriptor version (tcgen05)
+  desc |= static_cast<uint64_t>(ROW_BYTES == 128 ? 2 : 4) << 61;   // swizzle: 128 B / 64 B
   return desc;
 }
 
