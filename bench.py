@@ -67,10 +67,11 @@ def algorithmic_bytes(M, V, d, out_elt):
 # capture of the kernel sources with the given hash; reported only while the sources still match.
 # Entries: source hash -> {workload: bytes per launch (average over the workload's launches)}.
 MEASURED_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
-    #     -k regex:gather_gemm -s 9 -c 3 python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
-    # r_m 0.1 / 0.5 / 0.9 launches: 1.136 / 1.592 / 2.329 GB
-    "4c8f9c2fda282beb": {"llada8b": 1685530709},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,
+    #     lts__t_sector_hit_rate.pct --clock-control none -k regex:gather_gemm -s 9 -c 3
+    #     python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
+    # r_m 0.1 / 0.5 / 0.9 launches: 1.142 / 2.319 / 3.627 GB (mean per launch below)
+    "9606eb30d4e7d46b": {"llada8b": 2362691328},
 }
 
 
