@@ -260,7 +260,9 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     """The same step end to end through the public call: every step copies its inputs (H, idx,
     CSR offsets and W) from pinned host memory to the device and reads all logits back to pinned
     host memory. Uploads and read-backs run on their own streams and overlap compute and each
-    other (within and across steps); the timed region spans all of it."""
+    other (within and across steps); W has two device buffers, used by alternate steps, so one
+    step's W upload does not wait for the previous step's last member. The timed region spans all
+    of it."""
     import torch
 
     host_in, host_out = [], []
@@ -278,7 +280,10 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
         ho = torch.empty((c["mask"].M, c["w"].V), dtype=c["odt"], pin_memory=True)
         host_out.append(ho)
         d2h += ho.numel() * ho.element_size()
-    dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items()} for hi in host_in]
+    dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items() if k2 != "W"}
+              for hi in host_in]
+    dev_w = [[torch.empty_like(hi["W"], device=dev) if "W" in hi else None for hi in host_in]
+             for _ in range(2)]
     # one device output buffer per member so read-backs can overlap the next member's compute
     dev_out = [torch.empty_like(c["out"]) for c in calls]
     s_in = torch.cuda.Stream(device=dev)
@@ -288,22 +293,30 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     # its output buffer once its read-back is done. Nothing else is serialised, so uploads of
     # step k+1 overlap read-backs of step k (opposite directions, separate copy engines).
     consumed = [None] * len(calls)
+    w_consumed = [None, None]  # last use of each W buffer (the last member of its step)
     read_back = [None] * len(calls)
+    parity = [0]
 
     def e2e_step():
         Wd = None
+        wb = dev_w[parity[0]]
         for j, (c, hi, di, ho, do) in enumerate(zip(calls, host_in, dev_in, host_out, dev_out)):
             with torch.cuda.stream(s_in):
+                if "W" in hi:
+                    if w_consumed[parity[0]] is not None:
+                        s_in.wait_event(w_consumed[parity[0]])
+                    wb[j].copy_(hi["W"], non_blocking=True)
                 if consumed[j] is not None:
                     s_in.wait_event(consumed[j])
                 for k2, v in hi.items():
-                    di[k2].copy_(v, non_blocking=True)
+                    if k2 != "W":
+                        di[k2].copy_(v, non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(s_in)
             stream.wait_event(ready)
             if read_back[j] is not None:
                 stream.wait_event(read_back[j])
-            Wd = di.get("W", Wd)
+            Wd = wb[j] if "W" in hi else Wd
 
             def on_chunk(ci, rb, rows, out, ho=ho, c=c):
                 done = torch.cuda.Event()
@@ -322,8 +335,9 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
             consumed[j].record(stream)
             read_back[j] = torch.cuda.Event()
             read_back[j].record(s_out)
-        # W (member 0's input) is used by every member: not overwritten before the last is done
-        consumed[0] = consumed[-1]
+        # this step's W buffer is used by every member: not overwritten before the last is done
+        w_consumed[parity[0]] = consumed[-1]
+        parity[0] ^= 1
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -550,7 +564,7 @@ def main():
     ap.add_argument("--mode", default="logits", choices=["logits", "sample"],
                     help="logits: [M, V] mask-only logits (the metric); sample: fused greedy "
                          "sampling (token + confidence per masked row)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
