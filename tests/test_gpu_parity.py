@@ -61,6 +61,12 @@ def test_tiny_config_full_parity(mo):
     (4096, 4096, 2048, 1, torch.bfloat16),   # a single masked row
     (300, 64, 256, 257, torch.float32),      # one K block, exact N tile
     (2000, 1024, 8200, 700, torch.bfloat16), # many tiles: 6 x 33, persistent loop > 1 tile/CTA
+    # Schedule paths of the 256 x 512 pair units (76 pairs resident on a GB300):
+    (600, 256, 520, 300, torch.bfloat16),    # 3 panels: a one-panel unit column; 4 units, all
+                                             # split into halves, one half empty (skipped)
+    (2000, 256, 15104, 700, torch.bfloat16), # 3 x 30 units = 76 + 14: split last round, odd panels
+    (1500, 64, 16384, 1024, torch.bfloat16), # one K block (fewer than the stages) over 2 rounds
+    (1500, 128, 16384, 1024, torch.float32), # two K blocks, fp32 out
 ])
 def test_ragged_tiles_full_parity(mo, L, d, V, M, dt):
     H, W = rand_inputs(L, d, V, seed=L + d + V + M)

@@ -52,6 +52,8 @@ def check_against_logits(token, conf, logits):
     (777, 200, 520, 129),      # K tail, M tail
     (300, 64, 256, 100),       # single M tile (one CTA per tile)
     (2000, 1024, 8200, 700),
+    (600, 256, 520, 300),      # one-panel unit column, split last round with an empty half
+    (2000, 256, 15104, 700),   # 90 units over 76 pairs: split last round, odd panels
 ])
 def test_sample_matches_oracle(mo, L, d, V, M):
     H = wl.make_hidden(L, d, 3 + L, DEV)
