@@ -16,3 +16,9 @@ from .mask_only_logits import (  # noqa: F401
     resolve_rows,
     round_output,
 )
+from .fp8_logits import (  # noqa: F401
+    e4m3_bits_to_f64,
+    f64_to_e4m3_bits,
+    masked_logits_fp8,
+    quantize_rows,
+)
