@@ -117,6 +117,52 @@ MOSAIC_API mosaic_status mosaic_masked_logits(mosaic_handle* handle,
                                               void* user, void* stream);
 
 /*
+ * FP8 variant of mosaic_masked_logits: both operands in FP8 E4M3 ("fn": 1 sign, 4 exponent bits
+ * with bias 7, 3 fraction bits, largest finite 448) with one fp32 scale per row, so that
+ *
+ *     out[i, v] = hidden_scale[row(i)] * w_scale[v] * sum_k hidden_q[row(i), k] * W_q[v, k]
+ *
+ * accumulated in fp32 on the tensor cores (kind::f8f6f4) and stored as bf16 (round to nearest
+ * even) or fp32. The pages name FP8 for this step only as future work (the dLLM-Serve article
+ * "扩散大语言模型内存优化：从理论到系统设计", section 5) and give no scheme: the per-row scaling
+ * is this library's, and mosaic_quantize_rows_e4m3() produces operands in it.
+ *
+ * hidden_q      E4M3 codes [L_tot, d], one byte per element, row-major; 16-byte aligned.
+ * hidden_scale  fp32 [L_tot], 4-byte aligned.
+ * W_q           E4M3 codes [V, d]; 16-byte aligned.   w_scale  fp32 [V], 16-byte aligned.
+ * All other arguments, the chunking, the status word and the error behaviour are those of
+ * mosaic_masked_logits, except that d must be a multiple of 16 (16-byte rows of codes).
+ */
+MOSAIC_API mosaic_status mosaic_masked_logits_fp8(mosaic_handle* handle,
+                                                  const void* hidden_q, const float* hidden_scale,
+                                                  int64_t L_tot, int64_t d,
+                                                  const int32_t* mask_idx, int64_t M,
+                                                  const int32_t* seq_offsets,
+                                                  const int32_t* mask_offsets, int32_t B,
+                                                  const void* W_q, const float* w_scale,
+                                                  int64_t V, void* out, mosaic_dtype out_dtype,
+                                                  int64_t chunk_rows, mosaic_chunk_cb cb,
+                                                  void* user, void* stream);
+
+/*
+ * Per-row E4M3 quantization for mosaic_masked_logits_fp8 (no counterpart on the pages): for each
+ * row r of the bf16 matrix x [rows, d], a = max_k |x[r, k]|, scale[r] = a / 448 and
+ * q[r, k] = E4M3(x[r, k] * (448 / a)) rounded to nearest even and clamped to +-448, both
+ * divisions and the multiply single IEEE fp32 operations (so the result is a deterministic
+ * function of x); a row of zeros gets scale 0 and zero codes. Used once for W and per step for
+ * the hidden states.
+ *
+ * x      bf16 [rows, d] row-major, 16-byte aligned, device memory of the current device.
+ * q      E4M3 codes [rows, d] (one byte each), 16-byte aligned; caller-owned.
+ * scale  fp32 [rows], 4-byte aligned; caller-owned.
+ * Requirements (else MOSAIC_ERR_INVALID_ARG / MOSAIC_ERR_UNSUPPORTED, nothing enqueued):
+ * rows >= 0, d >= 1, d % 16 == 0, rows < 2^31. rows == 0 enqueues nothing. Enqueued on
+ * `stream` (cudaStream_t as void*).
+ */
+MOSAIC_API mosaic_status mosaic_quantize_rows_e4m3(const void* x, int64_t rows, int64_t d,
+                                                   void* q, float* scale, void* stream);
+
+/*
  * Synchronise `stream`, read and clear the handle's device status word. Returns MOSAIC_OK,
  * MOSAIC_ERR_INDEX (a bad mask index / CSR offsets were seen), MOSAIC_ERR_TIMEOUT (a bounded
  * wait inside a kernel gave up; the kernel returned and the CUDA context stays usable) or

@@ -26,6 +26,7 @@ struct mosaic_handle {
   int num_sms = 0;
   int max_clusters[2][2] = {};  // [out_f32][pair]: clusters resident at once
   int max_clusters_sample[2] = {};  // [pair], sampling epilogue
+  int max_clusters_fp8[2][2] = {};  // [out_f32][pair], FP8 operands
   uint32_t* d_status = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int64_t launches = 0;
@@ -99,10 +100,10 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* b
   return r == CUDA_SUCCESS;
 }
 
-// M units per raster group: as many as keep the group's gathered rows (cluster_m x BM x d
-// bf16 per unit) within ~64 MiB of L2, so that W panels are streamed once per group.
-int pick_group_u(int m_units, int cm, int64_t d) {
-  const int64_t per_unit = static_cast<int64_t>(cm) * mosaic::gather_gemm_block_m() * d * 2;
+// M units per raster group: as many as keep the group's gathered rows (cluster_m x BM rows of
+// row_bytes per unit) within ~64 MiB of L2, so that W panels are streamed once per group.
+int pick_group_u(int m_units, int cm, int64_t row_bytes) {
+  const int64_t per_unit = static_cast<int64_t>(cm) * mosaic::gather_gemm_block_m() * row_bytes;
   int64_t g = (64ll << 20) / per_unit;
   if (g < 1) g = 1;
   if (g > m_units) g = m_units;
@@ -169,6 +170,11 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
     e = mosaic::gather_gemm_prepare_sample(pair != 0, &h->max_clusters_sample[pair]);
     if (e == cudaSuccess && h->max_clusters_sample[pair] < 1) e = cudaErrorInvalidConfiguration;
   }
+  for (int f32 = 0; f32 < 2 && e == cudaSuccess; ++f32)
+    for (int pair = 0; pair < 2 && e == cudaSuccess; ++pair) {
+      e = mosaic::gather_gemm_prepare_fp8(f32 != 0, pair != 0, &h->max_clusters_fp8[f32][pair]);
+      if (e == cudaSuccess && h->max_clusters_fp8[f32][pair] < 1) e = cudaErrorInvalidConfiguration;
+    }
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e, "sampling kernel attributes / cluster occupancy");
@@ -219,12 +225,18 @@ mosaic_status mosaic_check(mosaic_handle* h, void* stream) {
   return MOSAIC_OK;
 }
 
-mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t L_tot,
-                                   int64_t d, const int32_t* mask_idx, int64_t M,
-                                   const int32_t* seq_offsets, const int32_t* mask_offsets,
-                                   int32_t B, const void* W, int64_t V, void* out,
-                                   mosaic_dtype out_dtype, int64_t chunk_rows,
-                                   mosaic_chunk_cb cb, void* user, void* stream_ptr) {
+}  // extern "C"
+
+namespace {
+
+// The lazy-chunk driver of mosaic_masked_logits and mosaic_masked_logits_fp8. fp8: hidden and W
+// hold E4M3 codes (one byte per element) with per-row scales h_scale [L_tot] and w_scale [V].
+mosaic_status logits_impl(mosaic_handle* h, const void* hidden, const float* h_scale,
+                          int64_t L_tot, int64_t d, const int32_t* mask_idx, int64_t M,
+                          const int32_t* seq_offsets, const int32_t* mask_offsets, int32_t B,
+                          const void* W, const float* w_scale, int64_t V, void* out,
+                          mosaic_dtype out_dtype, int64_t chunk_rows, mosaic_chunk_cb cb,
+                          void* user, void* stream_ptr, bool fp8) {
   if (!h) return fail(MOSAIC_ERR_INVALID_ARG, "NULL handle");
   if (M < 0) return fail(MOSAIC_ERR_INVALID_ARG, "M < 0");
   if (M >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "M >= 2^31");
@@ -246,17 +258,25 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
   if (V >= (1ll << 31) || d >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "V or d too large");
   if (!aligned16(hidden) || !aligned16(W) || !aligned16(out))
     return fail(MOSAIC_ERR_INVALID_ARG, "hidden, W and out must be 16-byte aligned");
+  if (fp8) {
+    if (d % 16 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 16 (16-byte E4M3 rows)");
+    if (!h_scale || !w_scale) return fail(MOSAIC_ERR_INVALID_ARG, "NULL hidden_scale or w_scale");
+    if (!aligned16(w_scale) || reinterpret_cast<uintptr_t>(h_scale) % 4 != 0)
+      return fail(MOSAIC_ERR_INVALID_ARG, "w_scale must be 16-byte aligned, hidden_scale 4-byte aligned");
+  }
 
   cudaError_t e = cudaSetDevice(h->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   if (!is_device_ptr(hidden, h->device) || !is_device_ptr(W, h->device) ||
       !is_device_ptr(out, h->device) || !is_device_ptr(mask_idx, h->device) ||
-      (csr && (!is_device_ptr(seq_offsets, h->device) || !is_device_ptr(mask_offsets, h->device))))
+      (csr && (!is_device_ptr(seq_offsets, h->device) || !is_device_ptr(mask_offsets, h->device))) ||
+      (fp8 && (!is_device_ptr(h_scale, h->device) || !is_device_ptr(w_scale, h->device))))
     return fail(MOSAIC_ERR_INVALID_ARG, "every array must be device memory of device %d", h->device);
 
   const bool f32 = out_dtype == MOSAIC_F32;
   const int BM = mosaic::gather_gemm_block_m(), BN = mosaic::gather_gemm_block_n(),
-            BK = mosaic::gather_gemm_block_k();
+            BK = fp8 ? mosaic::gather_gemm_block_k_fp8() : mosaic::gather_gemm_block_k();
+  const int elt = fp8 ? 1 : 2;
   const int64_t cr = chunked ? chunk_rows : M;
   const int64_t n_tiles = (V + BN - 1) / BN;
   const int64_t m_tiles_max = (cr + BM - 1) / BM;
@@ -267,8 +287,8 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
   const bool pair = m_tiles_max >= 2;
   const int cm = pair ? 2 : 1;
   CUtensorMap tm_w, tm_out;
-  if (!encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, V, d,
-                 mosaic::gather_gemm_w_box_rows(pair), BK))
+  if (!encode_2d(&tm_w, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 elt, W, V, d, mosaic::gather_gemm_w_box_rows(pair), BK))
     return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for W rejected");
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -297,15 +317,68 @@ mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t
     p.n_tiles = static_cast<int32_t>(n_tiles);
     p.cluster_m = cm;
     p.m_units = (p.m_tiles + cm - 1) / cm;
-    p.group_u = pick_group_u(p.m_units, cm, d);
+    p.group_u = pick_group_u(p.m_units, cm, d * elt);
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
-    const int grid = mosaic::gather_gemm_schedule(p, h->max_clusters[f32 ? 1 : 0][pair ? 1 : 0]);
-    e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
+    p.a_scale = h_scale;
+    p.b_scale = w_scale;
+    if (fp8) {
+      const int grid =
+          mosaic::gather_gemm_schedule(p, h->max_clusters_fp8[f32 ? 1 : 0][pair ? 1 : 0]);
+      e = mosaic::gather_gemm_launch_fp8(tm_w, tm_out, p, f32, grid, stream);
+    } else {
+      const int grid = mosaic::gather_gemm_schedule(p, h->max_clusters[f32 ? 1 : 0][pair ? 1 : 0]);
+      e = mosaic::gather_gemm_launch(tm_w, tm_out, p, f32, grid, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "gather-GEMM launch");
     ++h->launches;
     if (cb) cb(c, rb, rows, out, user);
   }
+  return MOSAIC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mosaic_status mosaic_masked_logits(mosaic_handle* h, const void* hidden, int64_t L_tot,
+                                   int64_t d, const int32_t* mask_idx, int64_t M,
+                                   const int32_t* seq_offsets, const int32_t* mask_offsets,
+                                   int32_t B, const void* W, int64_t V, void* out,
+                                   mosaic_dtype out_dtype, int64_t chunk_rows,
+                                   mosaic_chunk_cb cb, void* user, void* stream_ptr) {
+  return logits_impl(h, hidden, nullptr, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B, W,
+                     nullptr, V, out, out_dtype, chunk_rows, cb, user, stream_ptr, false);
+}
+
+mosaic_status mosaic_masked_logits_fp8(mosaic_handle* h, const void* hidden_q,
+                                       const float* hidden_scale, int64_t L_tot, int64_t d,
+                                       const int32_t* mask_idx, int64_t M,
+                                       const int32_t* seq_offsets, const int32_t* mask_offsets,
+                                       int32_t B, const void* W_q, const float* w_scale,
+                                       int64_t V, void* out, mosaic_dtype out_dtype,
+                                       int64_t chunk_rows, mosaic_chunk_cb cb, void* user,
+                                       void* stream_ptr) {
+  return logits_impl(h, hidden_q, hidden_scale, L_tot, d, mask_idx, M, seq_offsets, mask_offsets,
+                     B, W_q, w_scale, V, out, out_dtype, chunk_rows, cb, user, stream_ptr, true);
+}
+
+mosaic_status mosaic_quantize_rows_e4m3(const void* x, int64_t rows, int64_t d, void* q,
+                                        float* scale, void* stream_ptr) {
+  if (rows < 0 || d < 1) return fail(MOSAIC_ERR_INVALID_ARG, "rows < 0 or d < 1");
+  if (d % 16 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 16");
+  if (rows >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "rows >= 2^31");
+  if (rows == 0) return MOSAIC_OK;
+  if (!x || !q || !scale) return fail(MOSAIC_ERR_INVALID_ARG, "NULL x, q or scale");
+  if (!aligned16(x) || !aligned16(q) || reinterpret_cast<uintptr_t>(scale) % 4 != 0)
+    return fail(MOSAIC_ERR_INVALID_ARG, "x and q must be 16-byte aligned, scale 4-byte aligned");
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (!is_device_ptr(x, device) || !is_device_ptr(q, device) || !is_device_ptr(scale, device))
+    return fail(MOSAIC_ERR_INVALID_ARG, "x, q and scale must be device memory of the current device");
+  e = mosaic::quantize_rows_e4m3_launch(x, rows, d, q, scale, static_cast<cudaStream_t>(stream_ptr));
+  if (e != cudaSuccess) return cuda_fail(e, "quantization launch");
   return MOSAIC_OK;
 }
 
@@ -394,7 +467,7 @@ mosaic_status mosaic_masked_sample(mosaic_handle* h, const void* hidden, int64_t
     p.n_tiles = static_cast<int32_t>(n_tiles);
     p.cluster_m = cm;
     p.m_units = (p.m_tiles + cm - 1) / cm;
-    p.group_u = pick_group_u(p.m_units, cm, d);
+    p.group_u = pick_group_u(p.m_units, cm, d * 2);
     p.status = h->d_status;
     p.timeout_ns = h->timeout_ns;
     p.part_max = part_max;
@@ -552,7 +625,7 @@ mosaic_status mosaic_masked_logits_noalloc(const void* hidden, int64_t L_tot, in
     p.n_tiles = static_cast<int32_t>(n_tiles);
     p.cluster_m = cm;
     p.m_units = (p.m_tiles + cm - 1) / cm;
-    p.group_u = pick_group_u(p.m_units, cm, d);
+    p.group_u = pick_group_u(p.m_units, cm, d * 2);
     p.status = nd->status + c;  // this chunk's word of the fixed array
     p.timeout_ns = 2000000000ull;
     const int grid = mosaic::gather_gemm_schedule(p, nd->max_clusters[f32 ? 1 : 0][pair ? 1 : 0]);

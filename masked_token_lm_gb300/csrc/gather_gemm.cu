@@ -254,12 +254,18 @@ __device__ __forceinline__ Unit unit_of(int u, int rank, const GatherGemmParams&
   return t;
 }
 
-template <bool OUT_F32, bool PAIR, bool SAMPLE>
+// FP8: E4M3 operands (per-row scales applied in the epilogue): a K block is then 128 elements of
+// the same 128-byte rows, and the MMA is kind::f8f6f4 (K = 32 per instruction, 4 per K block).
+template <bool OUT_F32, bool PAIR, bool SAMPLE, bool FP8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gather_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                        const __grid_constant__ CUtensorMap tm_out,
                        const GatherGemmParams p) {
   using C = Cfg<PAIR>;
+  static_assert(!(FP8 && SAMPLE), "the sampling epilogue takes bf16 operands");
+  constexpr int BKE = FP8 ? ROW_BYTES : BK;   // elements per K block
+  constexpr int EPP = FP8 ? 16 : 8;           // elements per 16-byte piece
+  constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN) : C::IDESC;
   extern __shared__ uint8_t smem_raw[];
   Smem<PAIR> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -334,11 +340,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // and reports its bytes to the leader's barrier.
             if (leader) mbar_arrive_expect_tx(sm.full(stage), C::w_tx(t.nsub));
             for (int j = 0; j < t.nsub; ++j)
-              tma_load_2d_pair(sm.b(stage, j), &tm_w, kb * BK,
+              tma_load_2d_pair(sm.b(stage, j), &tm_w, kb * BKE,
                                (t.panel0 + j) * BN + rank * C::B_BOX_ROWS, full_c(stage), pol_w);
           } else {
             mbar_arrive_expect_tx(sm.full(stage), C::w_tx(1));
-            tma_load_2d(sm.b(stage), &tm_w, kb * BK, t.panel0 * BN, sm.full(stage), pol_w);
+            tma_load_2d(sm.b(stage), &tm_w, kb * BKE, t.panel0 * BN, sm.full(stage), pol_w);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -357,9 +363,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int ROW_STEP = A_THREADS / PIECES;
     const uint64_t pol_a = policy_evict_last();   // gathered rows are re-read by every N tile
     const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
-    const int64_t row_bytes = static_cast<int64_t>(p.d) * 2;
-    const int k_full = p.d / BK;                  // K blocks with every piece inside d
-    const bool tail_in = chunk * 8 < p.d % BK;    // this piece in the partial last K block
+    const int64_t row_bytes = static_cast<int64_t>(p.d) * (FP8 ? 1 : 2);
+    const int k_full = p.d / BKE;                 // K blocks with every piece inside d
+    const bool tail_in = chunk * EPP < p.d % BKE; // this piece in the partial last K block
     // The swizzle of TMA and of the MMA descriptors: the piece index (address bits 4..) is
     // XORed with address bits 7.. of the row start (64-byte rows: (row / 2) % 4; 128: row % 8).
     uint32_t dst_off[A_ROWS];
@@ -468,7 +474,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k) {
           // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
-          tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, C::IDESC, (kb | k) != 0 ? 1u : 0u);
+          if constexpr (FP8)
+            tc_mma_e4m3<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          else
+            tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
         }
       };
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
@@ -580,10 +589,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The row this thread stores is the same for every panel of the unit.
       const int r = tc.m * BM + row_in_tile;
       bool ok = true;
+      float sa = 0.0f;  // FP8: scale of this output row's hidden row
       if (r < p.rows) {
-        resolve_row(p, offs, p.row_begin + r, __ldg(p.idx + p.row_begin + r), ok);
+        const int32_t hr = resolve_row(p, offs, p.row_begin + r, __ldg(p.idx + p.row_begin + r), ok);
         if (!ok && half == 0) atomicOr(p.status, MOSAIC_STATUS_INDEX);
+        if constexpr (FP8) sa = __ldg(p.a_scale + hr);
       }
+      // FP8: the 4 column scales from column c (a multiple of 4; V % 8 == 0, so a group of 4 is
+      // either inside V or past it), times the row's scale.
+      auto col_scales = [&](int c, float* s4) {
+        const float4 w = c < p.V ? __ldg(reinterpret_cast<const float4*>(p.b_scale + c))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        s4[0] = sa * w.x; s4[1] = sa * w.y; s4[2] = sa * w.z; s4[3] = sa * w.w;
+      };
       for (int jp = 0; jp < tc.nsub; ++jp) {
         // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
         const int slot = PAIR ? jp : slot_next;
@@ -644,6 +662,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t v[32];
             tmem_ld_32x32b_x32(t_acc + c * 32, v);
             tmem_wait_ld();
+            if constexpr (FP8) {
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                float s4[4];
+                col_scales(n0 + c * 32 + 4 * g, s4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  v[4 * g + e] = __float_as_uint(__uint_as_float(v[4 * g + e]) * s4[e]);
+              }
+            }
             if (!ok) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;
@@ -655,15 +683,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // bf16 out: the half's 128 columns go to registers (rounded and packed) before any
           // store, so the slot is handed back after 4 TMEM loads rather than after the stores.
           uint32_t packed[2][32];
+          if constexpr (FP8) {
+            // 8 columns per load: the column scales add to the registers the packing holds
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(t_acc + q * 16, v);
-            tmem_wait_ld();
+            for (int q = 0; q < 16; ++q) {
+              uint32_t v[8];
+              tmem_ld_32x32b_x8(t_acc + q * 8, v);
+              float s8[8];
+              col_scales(n0 + q * 8, s8);
+              col_scales(n0 + q * 8 + 4, s8 + 4);
+              tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              packed[q >> 2][(q & 3) * 8 + j] =
-                  pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              for (int j = 0; j < 4; ++j)
+                packed[q >> 3][(q & 7) * 4 + j] =
+                    pack_bf16x2(__uint_as_float(v[2 * j]) * s8[2 * j],
+                                __uint_as_float(v[2 * j + 1]) * s8[2 * j + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(t_acc + q * 16, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                packed[q >> 2][(q & 3) * 8 + j] =
+                    pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            }
           }
           release_slot(slot);
           if (!ok) {
@@ -708,23 +754,24 @@ cudaLaunchConfig_t launch_config(int grid, cudaStream_t stream, cudaLaunchAttrib
   return cfg;
 }
 
-template <bool F32, bool PAIR, bool SAMPLE = false>
+template <bool F32, bool PAIR, bool SAMPLE = false, bool FP8 = false>
 cudaError_t prepare_one(int* clusters) {
-  cudaError_t e = cudaFuncSetAttribute(gather_gemm_kernel<F32, PAIR, SAMPLE>,
+  cudaError_t e = cudaFuncSetAttribute(gather_gemm_kernel<F32, PAIR, SAMPLE, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<PAIR>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<F32, PAIR>((PAIR ? 2 : 1) * 64, nullptr, attr);
-  return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR, SAMPLE>, &cfg);
+  return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR, SAMPLE, FP8>,
+                                        &cfg);
 }
 
-template <bool F32, bool PAIR, bool SAMPLE = false>
+template <bool F32, bool PAIR, bool SAMPLE = false, bool FP8 = false>
 cudaError_t launch_one(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                        const GatherGemmParams& p, int grid, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<F32, PAIR>(grid, stream, attr);
-  return cudaLaunchKernelEx(&cfg, gather_gemm_kernel<F32, PAIR, SAMPLE>, tm_w, tm_out, p);
+  return cudaLaunchKernelEx(&cfg, gather_gemm_kernel<F32, PAIR, SAMPLE, FP8>, tm_w, tm_out, p);
 }
 
 // One warp per row: lane l combines the row's partials of N tiles l, l + 32, ... (partials are
@@ -768,6 +815,7 @@ __global__ void sample_reduce_kernel(const GatherGemmParams p, int32_t* token, f
 int gather_gemm_block_m() { return BM; }
 int gather_gemm_block_n() { return BN; }
 int gather_gemm_block_k() { return BK; }
+int gather_gemm_block_k_fp8() { return ROW_BYTES; }
 int gather_gemm_epi_cols(bool out_f32) { return out_f32 ? 32 : 64; }
 int gather_gemm_w_box_rows(bool pair) {
   return pair ? Cfg<true>::B_BOX_ROWS : Cfg<false>::B_BOX_ROWS;
@@ -810,6 +858,25 @@ cudaError_t sample_reduce_launch(const GatherGemmParams& p, int32_t* token, floa
   const int blocks = (p.rows + threads / 32 - 1) / (threads / 32);
   sample_reduce_kernel<<<blocks, threads, 0, stream>>>(p, token, confidence);
   return cudaGetLastError();
+}
+
+cudaError_t gather_gemm_prepare_fp8(bool out_f32, bool pair, int* clusters) {
+  if (out_f32)
+    return pair ? prepare_one<true, true, false, true>(clusters)
+                : prepare_one<true, false, false, true>(clusters);
+  return pair ? prepare_one<false, true, false, true>(clusters)
+              : prepare_one<false, false, false, true>(clusters);
+}
+
+cudaError_t gather_gemm_launch_fp8(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
+                                   const GatherGemmParams& p, bool out_f32, int grid,
+                                   cudaStream_t stream) {
+  const bool pair = p.cluster_m == 2;
+  if (out_f32)
+    return pair ? launch_one<true, true, false, true>(tm_w, tm_out, p, grid, stream)
+                : launch_one<true, false, false, true>(tm_w, tm_out, p, grid, stream);
+  return pair ? launch_one<false, true, false, true>(tm_w, tm_out, p, grid, stream)
+              : launch_one<false, false, false, true>(tm_w, tm_out, p, grid, stream);
 }
 
 cudaError_t gather_gemm_prepare(bool out_f32, bool pair, int* clusters) {

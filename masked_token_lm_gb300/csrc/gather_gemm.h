@@ -44,11 +44,15 @@ struct GatherGemmParams {
   float* part_sum;              // sum over the tile's columns of exp(logit - part_max)
   int32_t* part_arg;            // first column of the maximum (-1: the row's index was bad)
   int32_t part_ld;
+  // FP8 variant only: per-row scales of the E4M3 operands (hidden rows [L_tot], W rows [V]).
+  const float* a_scale;
+  const float* b_scale;
 };
 
 int gather_gemm_block_m();
 int gather_gemm_block_n();
 int gather_gemm_block_k();
+int gather_gemm_block_k_fp8();  // E4M3 elements per K block
 int gather_gemm_epi_cols(bool out_f32);
 int gather_gemm_w_box_rows(bool pair);
 // Fills p.n_wide / units_full / units_total from p.m_units, p.n_tiles and p.cluster_m for a grid
@@ -67,5 +71,13 @@ cudaError_t sample_reduce_launch(const GatherGemmParams& p, int32_t* token, floa
 cudaError_t gather_gemm_launch(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
                                const GatherGemmParams& p, bool out_f32, int grid,
                                cudaStream_t stream);
+// FP8 variant: E4M3 hidden rows and W (tensor map of bytes), p.a_scale / p.b_scale per row.
+cudaError_t gather_gemm_prepare_fp8(bool out_f32, bool pair, int* clusters);
+cudaError_t gather_gemm_launch_fp8(const CUtensorMap& tm_w, const CUtensorMap& tm_out,
+                                   const GatherGemmParams& p, bool out_f32, int grid,
+                                   cudaStream_t stream);
+// Per-row E4M3 quantization of a bf16 [rows, d] matrix into codes [rows, d] and scales [rows].
+cudaError_t quantize_rows_e4m3_launch(const void* x, int64_t rows, int64_t d, void* q,
+                                      float* scale, cudaStream_t stream);
 
 }  // namespace mosaic

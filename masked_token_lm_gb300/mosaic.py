@@ -91,6 +91,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mosaic_workspace_reserved_bytes.restype = ctypes.c_int64
     lib.mosaic_workspace_destroy.argtypes = [P]
     lib.mosaic_workspace_destroy.restype = ctypes.c_int
+    lib.mosaic_masked_logits_fp8.argtypes = [P, P, P, I64, I64, P, I64, P, P, I32, P, P, I64, P,
+                                             ctypes.c_int, I64, mosaic_chunk_cb, P, P]
+    lib.mosaic_masked_logits_fp8.restype = ctypes.c_int
+    lib.mosaic_quantize_rows_e4m3.argtypes = [P, I64, I64, P, P, P]
+    lib.mosaic_quantize_rows_e4m3.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -115,6 +120,43 @@ def mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets, mas
     return load_library().mosaic_masked_logits(handle, hidden, L_tot, d, mask_idx, M, seq_offsets,
                                                mask_offsets, B, W, V, out, out_dtype, chunk_rows,
                                                cb_c, user, stream)
+
+
+def mosaic_masked_logits_fp8(handle, hidden_q, hidden_scale, L_tot, d, mask_idx, M, seq_offsets,
+                             mask_offsets, B, W_q, w_scale, V, out, out_dtype, chunk_rows, cb,
+                             user, stream) -> int:
+    """Raw call; pointer arguments are ints (device addresses) or None."""
+    cb_c = cb if isinstance(cb, mosaic_chunk_cb) else (mosaic_chunk_cb(cb) if cb else mosaic_chunk_cb())
+    return load_library().mosaic_masked_logits_fp8(handle, hidden_q, hidden_scale, L_tot, d,
+                                                   mask_idx, M, seq_offsets, mask_offsets, B,
+                                                   W_q, w_scale, V, out, out_dtype, chunk_rows,
+                                                   cb_c, user, stream)
+
+
+def mosaic_quantize_rows_e4m3(x, rows, d, q, scale, stream) -> int:
+    """Raw call; pointer arguments are ints (device addresses) or None."""
+    return load_library().mosaic_quantize_rows_e4m3(x, rows, d, q, scale, stream)
+
+
+def quantize_rows_e4m3(x, stream=None):
+    """Per-row E4M3 quantization of a contiguous bf16 [rows, d] tensor (see
+    mosaic_quantize_rows_e4m3 in include/mosaic.h). Returns (codes uint8 [rows, d],
+    scale float32 [rows]) on x's device; d must be a multiple of 16."""
+    import torch
+
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 [rows, d] tensor")
+    rows, d = int(x.shape[0]), int(x.shape[1])
+    q = torch.empty((rows, d), dtype=torch.uint8, device=x.device)
+    scale = torch.empty((rows,), dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        st = mosaic_quantize_rows_e4m3(x.data_ptr() if rows else None, rows, d,
+                                       q.data_ptr() if rows else None,
+                                       scale.data_ptr() if rows else None, s.cuda_stream)
+    if st != MOSAIC_OK:
+        raise MosaicError(st, mosaic_last_error_string())
+    return q, scale
 
 
 def mosaic_masked_logits_noalloc(hidden, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B,
@@ -238,6 +280,51 @@ class Mosaic:
             seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None, B,
             W.data_ptr(), V, out.data_ptr(), code, int(chunk_rows), cb, None,
             self._stream_ptr(stream))
+        if st != MOSAIC_OK:
+            raise MosaicError(st, mosaic_last_error_string())
+        return out
+
+    def masked_logits_fp8(self, hidden_q, hidden_scale, mask_idx, W_q, w_scale,
+                          seq_offsets=None, mask_offsets=None, out=None, out_dtype=None,
+                          chunk_rows: int = 0, on_chunk: Optional[Callable] = None, stream=None):
+        """FP8 variant of masked_logits: E4M3 codes (uint8 tensors) with per-row fp32 scales, as
+        produced by quantize_rows_e4m3; same chunking and output as masked_logits."""
+        import torch
+
+        for name, t, dt in (("hidden_q", hidden_q, torch.uint8), ("W_q", W_q, torch.uint8),
+                            ("hidden_scale", hidden_scale, torch.float32),
+                            ("w_scale", w_scale, torch.float32),
+                            ("mask_idx", mask_idx, torch.int32),
+                            ("seq_offsets", seq_offsets, torch.int32),
+                            ("mask_offsets", mask_offsets, torch.int32)):
+            if t is None:
+                continue
+            if t.dtype != dt or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {dt} tensor")
+        if hidden_q.dim() != 2 or W_q.dim() != 2 or hidden_q.shape[1] != W_q.shape[1]:
+            raise ValueError("hidden_q [L_tot, d] and W_q [V, d] must agree on d")
+        M = int(mask_idx.numel())
+        V, d = int(W_q.shape[0]), int(W_q.shape[1])
+        if out_dtype is None:
+            out_dtype = out.dtype if out is not None else torch.bfloat16
+        code = {torch.bfloat16: MOSAIC_BF16, torch.float32: MOSAIC_F32}[out_dtype]
+        chunked = 0 < chunk_rows < M
+        rows_out = chunk_rows if chunked else M
+        if out is None:
+            out = torch.empty((rows_out, V), dtype=out_dtype, device=W_q.device)
+        csr = seq_offsets is not None
+        B = int(seq_offsets.numel()) - 1 if csr else 0
+
+        def _cb(c, rb, rows, _ptr, _user):
+            on_chunk(int(c), int(rb), int(rows), out)
+
+        cb = mosaic_chunk_cb(_cb) if on_chunk is not None else mosaic_chunk_cb()
+        st = mosaic_masked_logits_fp8(
+            self.handle, hidden_q.data_ptr(), hidden_scale.data_ptr(), int(hidden_q.shape[0]), d,
+            mask_idx.data_ptr() if M > 0 else None, M,
+            seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None, B,
+            W_q.data_ptr(), w_scale.data_ptr(), V, out.data_ptr(), code, int(chunk_rows), cb,
+            None, self._stream_ptr(stream))
         if st != MOSAIC_OK:
             raise MosaicError(st, mosaic_last_error_string())
         return out
