@@ -436,6 +436,11 @@ def bench_cuda(args):
             ws_bytes = mz.mosaic_masked_sample_workspace_bytes(mask.M, w.V, w.chunk_rows)
             call["workspace"] = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
             tot_bytes += sample_bytes(mask.M, w.V, w.d, ws_bytes)
+        elif args.mode == "fp8":
+            # E4M3 W and gathered rows (1 byte), logits, indices, and the step's quantization of
+            # the masked hidden rows (bf16 read, codes and scales written)
+            tot_bytes += (w.V * w.d + mask.M * w.d + mask.M * w.V * out.element_size() + 4 * mask.M
+                          + mask.M * w.d * 3 + 4 * mask.M)
         else:
             tot_bytes += algorithmic_bytes(mask.M, w.V, w.d, out.element_size())
         calls.append(call)
@@ -444,11 +449,29 @@ def bench_cuda(args):
     for c in calls[1:]:
         if c["w"].V == calls[0]["w"].V and c["w"].d == calls[0]["w"].d:
             c["W"] = calls[0]["W"]
+    if args.mode == "fp8":
+        # W is quantized once (model load); each step quantizes the hidden rows it reads
+        for c in calls:
+            if c is calls[0] or c["W"] is not calls[0]["W"]:
+                c["Wq"], c["sW"] = mz.quantize_rows_e4m3(c["W"])
+            else:
+                c["Wq"], c["sW"] = calls[0]["Wq"], calls[0]["sW"]
+            c["Hq"] = torch.empty(c["H"].shape, dtype=torch.uint8, device=dev)
+            c["sH"] = torch.empty(c["H"].shape[0], dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
 
     noop = (lambda *a: None)
 
     def one_call(c):
         m = c["mask"]
+        if args.mode == "fp8":
+            # this step's hidden rows that the logits read, quantized in place
+            mz.quantize_masked_rows_e4m3(c["H"], m.idx, c["Hq"], c["sH"], m.seq_offsets,
+                                         m.mask_offsets, stream=stream)
+            mo.masked_logits_fp8(c["Hq"], c["sH"], m.idx, c["Wq"], c["sW"], m.seq_offsets,
+                                 m.mask_offsets, out=c["out"], chunk_rows=c["w"].chunk_rows,
+                                 on_chunk=noop if c["chunked"] else None, stream=stream)
+            return
         if args.mode == "sample":
             mo.masked_sample(c["H"], m.idx, c["W"], m.seq_offsets, m.mask_offsets,
                              chunk_rows=c["w"].chunk_rows, workspace=c["workspace"], stream=stream)
@@ -488,6 +511,8 @@ def bench_cuda(args):
         t_end.record(stream)
         torch.cuda.synchronize()
     launches = mo.launches - launches0
+    if args.mode == "fp8":
+        launches += args.steps * len(calls)  # one hidden-state quantization per call
     st = mo.check()
     if st != mz.MOSAIC_OK:
         raise SystemExit(f"kernel status {st}: {mz.mosaic_last_error_string()}")
@@ -511,12 +536,15 @@ def bench_cuda(args):
         cublas = bench_cublas_context(args, calls, tot_flops, stream)
 
     hbm, bf16, bf16_sus, peak_src = load_peaks()
+    # the contraction's own peak: E4M3 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)
+    tensor_peak = 2 * bf16 if args.mode == "fp8" else bf16
     kernel_tflops = tot_flops * args.steps / (kernel_ms * 1e-3) / 1e12
-    roof_time = max(tot_flops / (bf16 * 1e12), tot_bytes / (hbm * 1e9))
+    roof_time = max(tot_flops / (tensor_peak * 1e12), tot_bytes / (hbm * 1e9))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if args.mode == "fp8" else "bf16", "data": "synthetic",
         "config": {**describe(args.workload, ws),
                    "M": [c["mask"].M for c in calls],
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
@@ -526,13 +554,18 @@ def bench_cuda(args):
         "kernel_source_hash": kernel_source_hash(),
         "roofline_frac_of_step": roof_time / (ms_per_step * 1e-3) if world == 1 else None,
         "roofline": {
-            "bound": "tensor" if tot_flops / (bf16 * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm",
-            "achieved": kernel_tflops, "peak": bf16, "unit": "TFLOP/s",
-            "frac": kernel_tflops / bf16,
+            "bound": "tensor" if tot_flops / (tensor_peak * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm",
+            "achieved": kernel_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
+            "frac": kernel_tflops / tensor_peak,
             "traffic": (args.traffic if args.traffic is not None
-                        else MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(args.workload)),
-            "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback 1.9 PFLOP/s",
-            "kernel": "gather_gemm_kernel<false>", "achieved_gbs": tot_bytes * args.steps / (kernel_ms * 1e-3) / 1e9,
+                        else MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(args.workload)
+                        if args.mode == "logits" else None),
+            "peak_source": (f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                            else "fallback 1.9 PFLOP/s")
+                           + (" x 2 (nominal E4M3/bf16 ratio)" if args.mode == "fp8" else ""),
+            "kernel": ("gather_gemm_kernel<fp8> + per-step masked-row quantization"
+                       if args.mode == "fp8" else "gather_gemm_kernel<false>"),
+            "achieved_gbs": tot_bytes * args.steps / (kernel_ms * 1e-3) / 1e9,
             "hbm_peak_gbs": hbm,
         },
         "gpu_launches": launches,
@@ -561,9 +594,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llada8b")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--mode", default="logits", choices=["logits", "sample"],
+    ap.add_argument("--mode", default="logits", choices=["logits", "sample", "fp8"],
                     help="logits: [M, V] mask-only logits (the metric); sample: fused greedy "
-                         "sampling (token + confidence per masked row)")
+                         "sampling (token + confidence per masked row); fp8: the E4M3 variant "
+                         "(W quantized once, the masked hidden rows every step)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

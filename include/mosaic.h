@@ -163,6 +163,22 @@ MOSAIC_API mosaic_status mosaic_quantize_rows_e4m3(const void* x, int64_t rows, 
                                                    void* q, float* scale, void* stream);
 
 /*
+ * The same quantization applied only to the hidden rows a mosaic_masked_logits_fp8 call with
+ * the same (mask_idx, M, seq_offsets, mask_offsets, B) will read: for each masked position the
+ * row hidden[row] is quantized into hidden_q[row] / hidden_scale[row] ([L_tot, d] / [L_tot]
+ * buffers; the other rows are left as they are). Positions whose row is outside its sequence or
+ * outside hidden are skipped (the logits call reports them); duplicate positions write the same
+ * values. Argument rules as for mosaic_quantize_rows_e4m3 plus those of the mask arguments of
+ * mosaic_masked_logits; M == 0 enqueues nothing.
+ */
+MOSAIC_API mosaic_status mosaic_quantize_masked_rows_e4m3(const void* hidden, int64_t L_tot,
+                                                          int64_t d, const int32_t* mask_idx,
+                                                          int64_t M, const int32_t* seq_offsets,
+                                                          const int32_t* mask_offsets, int32_t B,
+                                                          void* hidden_q, float* hidden_scale,
+                                                          void* stream);
+
+/*
  * Synchronise `stream`, read and clear the handle's device status word. Returns MOSAIC_OK,
  * MOSAIC_ERR_INDEX (a bad mask index / CSR offsets were seen), MOSAIC_ERR_TIMEOUT (a bounded
  * wait inside a kernel gave up; the kernel returned and the CUDA context stays usable) or

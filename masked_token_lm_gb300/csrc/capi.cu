@@ -363,6 +363,40 @@ mosaic_status mosaic_masked_logits_fp8(mosaic_handle* h, const void* hidden_q,
                      B, W_q, w_scale, V, out, out_dtype, chunk_rows, cb, user, stream_ptr, true);
 }
 
+mosaic_status mosaic_quantize_masked_rows_e4m3(const void* hidden, int64_t L_tot, int64_t d,
+                                               const int32_t* mask_idx, int64_t M,
+                                               const int32_t* seq_offsets,
+                                               const int32_t* mask_offsets, int32_t B,
+                                               void* hidden_q, float* hidden_scale,
+                                               void* stream_ptr) {
+  if (M < 0 || L_tot < 1 || d < 1) return fail(MOSAIC_ERR_INVALID_ARG, "M < 0, L_tot < 1 or d < 1");
+  if (d % 16 != 0) return fail(MOSAIC_ERR_UNSUPPORTED, "d must be a multiple of 16");
+  if (M >= (1ll << 31) || L_tot >= (1ll << 31)) return fail(MOSAIC_ERR_UNSUPPORTED, "M or L_tot >= 2^31");
+  if ((seq_offsets == nullptr) != (mask_offsets == nullptr))
+    return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs both seq_offsets and mask_offsets");
+  const bool csr = seq_offsets != nullptr;
+  if (csr && B < 1) return fail(MOSAIC_ERR_INVALID_ARG, "CSR mode needs B >= 1");
+  if (M == 0) return MOSAIC_OK;
+  if (!hidden || !mask_idx || !hidden_q || !hidden_scale)
+    return fail(MOSAIC_ERR_INVALID_ARG, "NULL hidden, mask_idx, hidden_q or hidden_scale");
+  if (!aligned16(hidden) || !aligned16(hidden_q) || reinterpret_cast<uintptr_t>(hidden_scale) % 4 != 0)
+    return fail(MOSAIC_ERR_INVALID_ARG, "hidden and hidden_q must be 16-byte aligned, hidden_scale 4-byte aligned");
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (!is_device_ptr(hidden, device) || !is_device_ptr(mask_idx, device) ||
+      !is_device_ptr(hidden_q, device) || !is_device_ptr(hidden_scale, device) ||
+      (csr && (!is_device_ptr(seq_offsets, device) || !is_device_ptr(mask_offsets, device))))
+    return fail(MOSAIC_ERR_INVALID_ARG, "every array must be device memory of the current device");
+  e = mosaic::quantize_masked_rows_e4m3_launch(hidden, L_tot, d, mask_idx, M,
+                                               csr ? seq_offsets : nullptr,
+                                               csr ? mask_offsets : nullptr, csr ? B : 0,
+                                               hidden_q, hidden_scale,
+                                               static_cast<cudaStream_t>(stream_ptr));
+  if (e != cudaSuccess) return cuda_fail(e, "quantization launch");
+  return MOSAIC_OK;
+}
+
 mosaic_status mosaic_quantize_rows_e4m3(const void* x, int64_t rows, int64_t d, void* q,
                                         float* scale, void* stream_ptr) {
   if (rows < 0 || d < 1) return fail(MOSAIC_ERR_INVALID_ARG, "rows < 0 or d < 1");

@@ -79,5 +79,12 @@ cudaError_t gather_gemm_launch_fp8(const CUtensorMap& tm_w, const CUtensorMap& t
 // Per-row E4M3 quantization of a bf16 [rows, d] matrix into codes [rows, d] and scales [rows].
 cudaError_t quantize_rows_e4m3_launch(const void* x, int64_t rows, int64_t d, void* q,
                                       float* scale, cudaStream_t stream);
+// The same for only the hidden rows of masked positions 0..n-1 (flat or CSR, as in the logits
+// call); other rows of q / scale are left as they are, out-of-range positions are skipped.
+cudaError_t quantize_masked_rows_e4m3_launch(const void* x, int64_t L_tot, int64_t d,
+                                             const int32_t* idx, int64_t n,
+                                             const int32_t* seq_offsets,
+                                             const int32_t* mask_offsets, int32_t B, void* q,
+                                             float* scale, cudaStream_t stream);
 
 }  // namespace mosaic

@@ -96,6 +96,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mosaic_masked_logits_fp8.restype = ctypes.c_int
     lib.mosaic_quantize_rows_e4m3.argtypes = [P, I64, I64, P, P, P]
     lib.mosaic_quantize_rows_e4m3.restype = ctypes.c_int
+    lib.mosaic_quantize_masked_rows_e4m3.argtypes = [P, I64, I64, P, I64, P, P, I32, P, P, P]
+    lib.mosaic_quantize_masked_rows_e4m3.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -136,6 +138,35 @@ def mosaic_masked_logits_fp8(handle, hidden_q, hidden_scale, L_tot, d, mask_idx,
 def mosaic_quantize_rows_e4m3(x, rows, d, q, scale, stream) -> int:
     """Raw call; pointer arguments are ints (device addresses) or None."""
     return load_library().mosaic_quantize_rows_e4m3(x, rows, d, q, scale, stream)
+
+
+def mosaic_quantize_masked_rows_e4m3(hidden, L_tot, d, mask_idx, M, seq_offsets, mask_offsets, B,
+                                     hidden_q, hidden_scale, stream) -> int:
+    """Raw call; pointer arguments are ints (device addresses) or None."""
+    return load_library().mosaic_quantize_masked_rows_e4m3(hidden, L_tot, d, mask_idx, M,
+                                                           seq_offsets, mask_offsets, B, hidden_q,
+                                                           hidden_scale, stream)
+
+
+def quantize_masked_rows_e4m3(hidden, mask_idx, hidden_q, hidden_scale, seq_offsets=None,
+                              mask_offsets=None, stream=None):
+    """Quantize, in place in hidden_q (uint8 [L_tot, d]) / hidden_scale (float32 [L_tot]), the
+    hidden rows the masked positions name (see mosaic_quantize_masked_rows_e4m3)."""
+    import torch
+
+    L_tot, d = int(hidden.shape[0]), int(hidden.shape[1])
+    M = int(mask_idx.numel())
+    csr = seq_offsets is not None
+    s = stream if stream is not None else torch.cuda.current_stream(hidden.device)
+    with torch.cuda.device(hidden.device):
+        st = mosaic_quantize_masked_rows_e4m3(
+            hidden.data_ptr(), L_tot, d, mask_idx.data_ptr() if M else None, M,
+            seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None,
+            int(seq_offsets.numel()) - 1 if csr else 0, hidden_q.data_ptr(),
+            hidden_scale.data_ptr(), s.cuda_stream)
+    if st != MOSAIC_OK:
+        raise MosaicError(st, mosaic_last_error_string())
+    return hidden_q, hidden_scale
 
 
 def quantize_rows_e4m3(x, stream=None):

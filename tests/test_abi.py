@@ -31,7 +31,8 @@ def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "mosaic_check", "mosaic_create", "mosaic_destroy", "mosaic_last_error_string",
         "mosaic_launch_count", "mosaic_masked_logits", "mosaic_masked_logits_fp8",
-        "mosaic_masked_logits_noalloc", "mosaic_quantize_rows_e4m3",
+        "mosaic_masked_logits_noalloc", "mosaic_quantize_masked_rows_e4m3",
+        "mosaic_quantize_rows_e4m3",
         "mosaic_masked_sample", "mosaic_masked_sample_workspace_bytes", "mosaic_min_chunk_rows",
         "mosaic_set_wait_timeout", "mosaic_workspace_bind", "mosaic_workspace_bound_bytes",
         "mosaic_workspace_create", "mosaic_workspace_destroy", "mosaic_workspace_reserved_bytes",

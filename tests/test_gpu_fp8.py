@@ -135,6 +135,37 @@ def test_fp8_chunked_equals_unchunked_bitwise(mo, chunk_rows):
     assert torch.equal(got, full)
 
 
+@pytest.mark.parametrize("csr", [False, True])
+def test_quantize_masked_rows_touches_only_the_masked_rows(csr):
+    d = 256
+    if csr:
+        m = wl.ragged_mask(5, 200, seed=4)
+        L = int(m.seq_offsets[-1])
+        idx, so, mo_ = m.idx, m.seq_offsets, m.mask_offsets
+        rows = np.concatenate([
+            so[b].item() + idx[mo_[b]:mo_[b + 1]].numpy() for b in range(5)])
+    else:
+        L = 700
+        g = torch.Generator().manual_seed(8)
+        idx = torch.randint(0, L, (300,), generator=g, dtype=torch.int32)  # with duplicates
+        idx[7] = 10 ** 6                                                   # out of range: skipped
+        so = mo_ = None
+        rows = idx.numpy()[idx.numpy() < L]
+    H = wl.make_hidden(L, d, 12, DEV)
+    q = torch.full((L, d), 0xAB, dtype=torch.uint8, device=DEV)
+    s = torch.full((L,), -1.0, dtype=torch.float32, device=DEV)
+    mz.quantize_masked_rows_e4m3(H, idx.to(DEV), q, s, so.to(DEV) if csr else None,
+                                 mo_.to(DEV) if csr else None)
+    torch.cuda.synchronize()
+    q_ref, s_ref = f8.quantize_rows(bits(H.cpu()))
+    qc, sc = q.cpu().numpy(), s.cpu().numpy()
+    touched = np.zeros(L, bool)
+    touched[rows] = True
+    assert np.array_equal(qc[touched], q_ref[touched])
+    assert np.array_equal(sc[touched].view(np.uint32), s_ref[touched].view(np.uint32))
+    assert np.all(qc[~touched] == 0xAB) and np.all(sc[~touched] == -1.0)
+
+
 def test_fp8_argument_errors():
     x = torch.zeros((4, 24), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(mz.MosaicError):
