@@ -683,30 +683,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // bf16 out: the half's 128 columns go to registers (rounded and packed) before any
           // store, so the slot is handed back after 4 TMEM loads rather than after the stores.
           uint32_t packed[2][32];
-          if constexpr (FP8) {
-            // 8 columns per load: the column scales add to the registers the packing holds
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              uint32_t v[8];
-              tmem_ld_32x32b_x8(t_acc + q * 8, v);
-              float s8[8];
-              col_scales(n0 + q * 8, s8);
-              col_scales(n0 + q * 8 + 4, s8 + 4);
-              tmem_wait_ld();
+          for (int q = 0; q < 8; ++q) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(t_acc + q * 16, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                packed[q >> 3][(q & 7) * 4 + j] =
-                    pack_bf16x2(__uint_as_float(v[2 * j]) * s8[2 * j],
-                                __uint_as_float(v[2 * j + 1]) * s8[2 * j + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint32_t v[16];
-              tmem_ld_32x32b_x16(t_acc + q * 16, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 8; ++j) {
+              if constexpr (FP8)  // the row's scale here; the columns' after the slot is free
+                packed[q >> 2][(q & 3) * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sa,
+                                                              __uint_as_float(v[2 * j + 1]) * sa);
+              else
                 packed[q >> 2][(q & 3) * 8 + j] =
                     pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
             }
@@ -716,7 +703,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) { packed[0][j] = 0u; packed[1][j] = 0u; }
           }
+          // FP8: W's column scales, applied to the rounded values (a second bf16 rounding)
+          auto scale_cols = [&](uint32_t (&w32)[32], int c0) {
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+              const int c = c0 + 4 * g;
+              const float4 w = c < p.V ? __ldg(reinterpret_cast<const float4*>(p.b_scale + c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+              uint32_t& a = w32[2 * g];
+              uint32_t& b = w32[2 * g + 1];
+              a = pack_bf16x2(__uint_as_float(a << 16) * w.x, __uint_as_float(a & 0xffff0000u) * w.y);
+              b = pack_bf16x2(__uint_as_float(b << 16) * w.z, __uint_as_float(b & 0xffff0000u) * w.w);
+            }
+          };
+          if constexpr (FP8) scale_cols(packed[0], n0);
           stage_store(packed[0], n0, tc.m);
+          if constexpr (FP8) scale_cols(packed[1], n0 + 64);
           stage_store(packed[1], n0 + 64, tc.m);
         }
       }  // panels of the unit
