@@ -29,7 +29,7 @@
 // 256-column panel, each into its own TMEM slot, issued by the leader CTA. Each CTA gathers its
 // own 128 A rows and loads its own 128-row half of each panel's W rows, so per K block an SM
 // takes in 16 KiB of gathered rows and 32 KiB of W for 2 x 2^22 FLOP: 48 bytes per tensor-core
-// cycle (a 256 x 256 unit needs 64 and measured ~81 % tensor-pipe busy against ~89 % for this).
+// cycle (a 256 x 256 unit needs 64 and measured ~81 % tensor-pipe busy; this form ~92 %).
 // The leader's stage barriers collect the whole pair: its W expect_tx covers the boxes of both
 // CTAs (each CTA's cta_group::2 TMA load reports its bytes there), and each CTA's relay reports
 // its own gathered rows. Commits multicast to both CTAs. The slots are drained one after the
