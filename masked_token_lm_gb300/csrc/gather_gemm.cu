@@ -562,6 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // one TMA store of the buffer (rows past the chunk are clipped by the tensor map).
     auto stage_store = [&](const uint32_t (&w)[32], int x, int m_tile) {
       if (gt == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
+      __syncwarp();  // the named barriers are warp-aligned: reconverge after the one-lane wait
       named_bar_sync(bar_half, EPI_THREADS / 2);
       const uint32_t dst = stage_buf + row_in_tile * 128;
       const int sw = row_in_tile & 7;
@@ -608,6 +609,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!PAIR) slot_next ^= 1;
         if (et == 0)
           *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
+        __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
         named_bar_sync(1, EPI_THREADS);
         if (!*sm.epi_go()) { go = false; break; }
         tc_fence_after();
@@ -724,6 +726,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }  // panels of the unit
     }
     if (gt == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before();

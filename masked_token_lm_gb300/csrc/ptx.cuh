@@ -388,6 +388,9 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// Named barrier over `nthreads` threads (whole warps). bar.sync is warp-aligned: every thread of
+// a warp must reach it together, so a warp whose lanes diverged (one lane waiting on an mbarrier)
+// reconverges with __syncwarp() first.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
