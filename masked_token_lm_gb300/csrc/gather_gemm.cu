@@ -100,7 +100,7 @@ struct Cfg {
   // full, empty, afull (peer gather -> relay), tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 3 * STAGES + 5;
   static constexpr int SMEM_MISC_OFF = (SMEM_BAR_OFF + NUM_BARS * 8 + 15) / 16 * 16;
-  // misc: tmem slot, abort flag, epilogue verdict, pad; 16-byte relay signal slot
+  // misc: tmem slot, abort flag, epilogue go flag, pad; 16-byte relay signal slot
   static constexpr int SMEM_OFFS_OFF = SMEM_MISC_OFF + 32;  // seq_offsets, mask_offsets copies
   static constexpr int SMEM_BYTES = SMEM_OFFS_OFF + 2 * OFFS_CAP * 4 + 1024;  // + alignment slack
   // Arrivals per phase on the (leader's) full barrier: its W expect_tx and its relay's arrive
