@@ -70,8 +70,8 @@ MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,
     #     lts__t_sector_hit_rate.pct --clock-control none -k regex:gather_gemm -s 9 -c 3
     #     python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
-    # r_m 0.1 / 0.5 / 0.9 launches: 1.136 / 1.670 / 2.599 GB (mean per launch below)
-    "3abc55336eb247d1": {"llada8b": 1801842347},
+    # r_m 0.1 / 0.5 / 0.9 launches: 1.137 / 1.859 / 2.763 GB (mean per launch below)
+    "efb394bd87f06b2b": {"llada8b": 1919696469},
 }
 
 
