@@ -58,6 +58,7 @@ def test_quantize_rows_is_bitwise_the_oracle(rows, d, scale):
     (1000, 512, 1000, 300, torch.float32),
     (777, 144, 520, 129, torch.bfloat16),     # K tail (144 = 128 + 16), M tail of one row
     (300, 128, 256, 100, torch.bfloat16),     # one M tile: single CTA, one K block
+    (300, 272, 264, 100, torch.float32),      # single CTA, fp32 out, K tail, N tail of 8 columns
     (600, 256, 520, 300, torch.bfloat16),     # one-panel unit column, split last round
     (2000, 1024, 8200, 700, torch.bfloat16),  # many units, persistent loop
 ])
