@@ -177,7 +177,7 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
     }
   if (e != cudaSuccess) {
     delete h;
-    return cuda_fail(e, "sampling kernel attributes / cluster occupancy");
+    return cuda_fail(e, "sampling / FP8 kernel attributes, cluster occupancy");
   }
   e = cudaMalloc(&h->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 256);
@@ -299,7 +299,7 @@ mosaic_status logits_impl(mosaic_handle* h, const void* hidden, const float* h_s
     const CUtensorMapDataType odt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!encode_2d(&tm_out, odt, f32 ? 4 : 2, out, rows, V, BM, mosaic::gather_gemm_epi_cols(f32)))
       return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for out rejected");
-    mosaic::GatherGemmParams p;
+    mosaic::GatherGemmParams p = {};  // fields a variant does not use stay null
     p.hidden = hidden;
     p.idx = mask_idx;
     p.seq_offsets = csr ? seq_offsets : nullptr;
@@ -641,7 +641,7 @@ mosaic_status mosaic_masked_logits_noalloc(const void* hidden, int64_t L_tot, in
     const CUtensorMapDataType odt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (!encode_2d(&tm_out, odt, f32 ? 4 : 2, out, rows, V, BM, mosaic::gather_gemm_epi_cols(f32)))
       return fail(MOSAIC_ERR_UNSUPPORTED, "tensor map for out rejected");
-    mosaic::GatherGemmParams p;
+    mosaic::GatherGemmParams p = {};  // fields a variant does not use stay null
     p.hidden = hidden;
     p.idx = mask_idx;
     p.seq_offsets = csr ? seq_offsets : nullptr;

@@ -154,7 +154,13 @@ def quantize_masked_rows_e4m3(hidden, mask_idx, hidden_q, hidden_scale, seq_offs
     hidden rows the masked positions name (see mosaic_quantize_masked_rows_e4m3)."""
     import torch
 
+    if hidden.dim() != 2:
+        raise ValueError("hidden must be [L_tot, d]")
     L_tot, d = int(hidden.shape[0]), int(hidden.shape[1])
+    _require("hidden", hidden, torch.bfloat16)
+    _require("hidden_q", hidden_q, torch.uint8, (L_tot, d))
+    _require("hidden_scale", hidden_scale, torch.float32, (L_tot,))
+    _check_mask(mask_idx, seq_offsets, mask_offsets)
     M = int(mask_idx.numel())
     csr = seq_offsets is not None
     s = stream if stream is not None else torch.cuda.current_stream(hidden.device)
@@ -239,6 +245,46 @@ def mosaic_last_error_string() -> str:
     return load_library().mosaic_last_error_string().decode()
 
 
+# ------------------------------------------------------------------ host-side argument checks
+# The kernels read and write exactly the extents the sizes passed to the C ABI imply; the library
+# cannot see a tensor's real size, so the wrappers check every tensor against those extents here.
+
+def _require(name, t, dtype, shape=None):
+    """t must be a contiguous tensor of `dtype` (and of exactly `shape`, if given)."""
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check_mask(mask_idx, seq_offsets, mask_offsets):
+    """mask_idx int32 [M]; the CSR pair both or neither, int32 [B + 1] each with B >= 1.
+    Returns B (0 in flat mode)."""
+    import torch
+
+    _require("mask_idx", mask_idx, torch.int32)
+    if mask_idx.dim() != 1:
+        raise ValueError("mask_idx must be one-dimensional")
+    if (seq_offsets is None) != (mask_offsets is None):
+        raise ValueError("CSR mode needs both seq_offsets and mask_offsets")
+    if seq_offsets is None:
+        return 0
+    _require("seq_offsets", seq_offsets, torch.int32)
+    _require("mask_offsets", mask_offsets, torch.int32)
+    if seq_offsets.dim() != 1 or mask_offsets.shape != seq_offsets.shape or seq_offsets.numel() < 2:
+        raise ValueError("seq_offsets and mask_offsets must both be int32 [B + 1] with B >= 1")
+    return int(seq_offsets.numel()) - 1
+
+
+def _check_out(out, rows_out, V, out_dtype):
+    import torch
+
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be torch.bfloat16 or torch.float32")
+    if out is not None:
+        _require("out", out, out_dtype, (rows_out, V))
+
+
 # ------------------------------------------------------------------ torch convenience wrapper
 
 class Mosaic:
@@ -264,11 +310,10 @@ class Mosaic:
         except Exception:
             pass
 
-    @staticmethod
-    def _stream_ptr(stream):
+    def _stream_ptr(self, stream):
         import torch
 
-        s = stream if stream is not None else torch.cuda.current_stream()
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
         return s.cuda_stream
 
     def masked_logits(self, hidden, mask_idx, W, seq_offsets=None, mask_offsets=None,
@@ -279,27 +324,22 @@ class Mosaic:
         each chunk is enqueued; it must enqueue its use of ``out`` on the same stream."""
         import torch
 
-        for name, t, dt in (("hidden", hidden, torch.bfloat16), ("W", W, torch.bfloat16),
-                            ("mask_idx", mask_idx, torch.int32),
-                            ("seq_offsets", seq_offsets, torch.int32),
-                            ("mask_offsets", mask_offsets, torch.int32)):
-            if t is None:
-                continue
-            if t.dtype != dt or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous {dt} tensor")
+        _require("hidden", hidden, torch.bfloat16)
+        _require("W", W, torch.bfloat16)
         if hidden.dim() != 2 or W.dim() != 2 or hidden.shape[1] != W.shape[1]:
             raise ValueError("hidden [L_tot, d] and W [V, d] must agree on d")
+        B = _check_mask(mask_idx, seq_offsets, mask_offsets)
         M = int(mask_idx.numel())
         V, d = int(W.shape[0]), int(W.shape[1])
         if out_dtype is None:
             out_dtype = out.dtype if out is not None else torch.bfloat16
-        code = {torch.bfloat16: MOSAIC_BF16, torch.float32: MOSAIC_F32}[out_dtype]
         chunked = 0 < chunk_rows < M
         rows_out = chunk_rows if chunked else M
+        _check_out(out, rows_out, V, out_dtype)
+        code = MOSAIC_F32 if out_dtype == torch.float32 else MOSAIC_BF16
         if out is None:
             out = torch.empty((rows_out, V), dtype=out_dtype, device=W.device)
         csr = seq_offsets is not None
-        B = int(seq_offsets.numel()) - 1 if csr else 0
 
         def _cb(c, rb, rows, _ptr, _user):
             on_chunk(int(c), int(rb), int(rows), out)
@@ -322,29 +362,24 @@ class Mosaic:
         produced by quantize_rows_e4m3; same chunking and output as masked_logits."""
         import torch
 
-        for name, t, dt in (("hidden_q", hidden_q, torch.uint8), ("W_q", W_q, torch.uint8),
-                            ("hidden_scale", hidden_scale, torch.float32),
-                            ("w_scale", w_scale, torch.float32),
-                            ("mask_idx", mask_idx, torch.int32),
-                            ("seq_offsets", seq_offsets, torch.int32),
-                            ("mask_offsets", mask_offsets, torch.int32)):
-            if t is None:
-                continue
-            if t.dtype != dt or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous {dt} tensor")
+        _require("hidden_q", hidden_q, torch.uint8)
+        _require("W_q", W_q, torch.uint8)
         if hidden_q.dim() != 2 or W_q.dim() != 2 or hidden_q.shape[1] != W_q.shape[1]:
             raise ValueError("hidden_q [L_tot, d] and W_q [V, d] must agree on d")
+        _require("hidden_scale", hidden_scale, torch.float32, (hidden_q.shape[0],))
+        _require("w_scale", w_scale, torch.float32, (W_q.shape[0],))
+        B = _check_mask(mask_idx, seq_offsets, mask_offsets)
         M = int(mask_idx.numel())
         V, d = int(W_q.shape[0]), int(W_q.shape[1])
         if out_dtype is None:
             out_dtype = out.dtype if out is not None else torch.bfloat16
-        code = {torch.bfloat16: MOSAIC_BF16, torch.float32: MOSAIC_F32}[out_dtype]
         chunked = 0 < chunk_rows < M
         rows_out = chunk_rows if chunked else M
+        _check_out(out, rows_out, V, out_dtype)
+        code = MOSAIC_F32 if out_dtype == torch.float32 else MOSAIC_BF16
         if out is None:
             out = torch.empty((rows_out, V), dtype=out_dtype, device=W_q.device)
         csr = seq_offsets is not None
-        B = int(seq_offsets.numel()) - 1 if csr else 0
 
         def _cb(c, rb, rows, _ptr, _user):
             on_chunk(int(c), int(rb), int(rows), out)
@@ -367,21 +402,29 @@ class Mosaic:
         not given."""
         import torch
 
+        _require("hidden", hidden, torch.bfloat16)
+        _require("W", W, torch.bfloat16)
+        if hidden.dim() != 2 or W.dim() != 2 or hidden.shape[1] != W.shape[1]:
+            raise ValueError("hidden [L_tot, d] and W [V, d] must agree on d")
+        B = _check_mask(mask_idx, seq_offsets, mask_offsets)
         M = int(mask_idx.numel())
         V, d = int(W.shape[0]), int(W.shape[1])
-        token = torch.empty(M, dtype=torch.int32, device=W.device)
-        conf = torch.empty(M, dtype=torch.float32, device=W.device)
         need = mosaic_masked_sample_workspace_bytes(M, V, chunk_rows)
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
+        elif not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor")
+        token = torch.empty(M, dtype=torch.int32, device=W.device)
+        conf = torch.empty(M, dtype=torch.float32, device=W.device)
         csr = seq_offsets is not None
         st = mosaic_masked_sample(
             self.handle, hidden.data_ptr(), int(hidden.shape[0]), d,
             mask_idx.data_ptr() if M > 0 else None, M,
             seq_offsets.data_ptr() if csr else None, mask_offsets.data_ptr() if csr else None,
-            int(seq_offsets.numel()) - 1 if csr else 0, W.data_ptr(), V,
+            B, W.data_ptr(), V,
             token.data_ptr() if M > 0 else None, conf.data_ptr() if M > 0 else None,
-            workspace.data_ptr(), workspace.numel(), int(chunk_rows), self._stream_ptr(stream))
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(chunk_rows),
+            self._stream_ptr(stream))
         if st != MOSAIC_OK:
             raise MosaicError(st, mosaic_last_error_string())
         return token, conf
