@@ -230,6 +230,26 @@ class CpuOracleTimer:
         return (f"oracle (bf16 decode + fp64 gather and matmul, numpy/OpenBLAS) on the first "
                 f"{self.n} masked rows of {self.w.name}, all V={self.w.V} columns; per call")
 
+    @staticmethod
+    def cpu():
+        """The host CPU: architecture, model (or ARM part number) and logical cores."""
+        import platform
+
+        model = ""
+        try:
+            with open("/proc/cpuinfo", encoding="utf-8") as f:
+                info = f.read()
+            for key in ("model name", "CPU part"):
+                for line in info.splitlines():
+                    if line.startswith(key):
+                        model = f"{key} {line.split(':', 1)[1].strip()}"
+                        break
+                if model:
+                    break
+        except OSError:
+            pass
+        return f"{platform.machine()}, {model or 'model unknown'}, {os.cpu_count()} logical cores"
+
 
 def bench_reference(args):
     world, rank, _ = dist_setup()
@@ -254,7 +274,7 @@ def bench_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": describe(args.workload, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
-                         "sample": timer.sample()},
+                         "sample": timer.sample(), "cpu": timer.cpu()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -583,7 +603,7 @@ def bench_cuda(args):
         timer.calibrate(args.ref_step_s)
         v, secs = timer.run()
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
-                                "sample": timer.sample(), "seconds": secs}
+                                "sample": timer.sample(), "seconds": secs, "cpu": timer.cpu()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     mo.close()

@@ -52,6 +52,13 @@ def test_tiny_config_full_parity(mo):
     out = run(mo, H, mask.idx.to(DEV), W, torch.float32)
     ref = orc.masked_logits(bits(H), mask.idx.numpy(), bits(W))
     assert_close(out, ref, torch.float32, "tiny")
+    # lazy chunking on the same workload: 128 one-row launches, 19 launches of 7 rows, and
+    # chunk_rows = M (chunking stays off); each equals the unchunked call bit for bit
+    for chunk_rows in (1, 7, 128):
+        before = mo.launches
+        ch = run(mo, H, mask.idx.to(DEV), W, torch.float32, chunk_rows=chunk_rows)
+        assert mo.launches - before == -(-mask.M // chunk_rows)
+        assert torch.equal(ch.view(torch.int32), out.view(torch.int32)), chunk_rows
 
 
 @pytest.mark.parametrize("L,d,V,M,dt", [
