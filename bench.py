@@ -213,10 +213,16 @@ class CpuOracleTimer:
         self.n = None
 
     def calibrate(self, target_s):
-        t0 = time.perf_counter()
-        self.orc.masked_logits(self.Hb, self.rows[:8], self.Wb)
-        dt = time.perf_counter() - t0
-        self.n = int(max(8, min(len(self.rows), 8 * target_s / max(dt, 1e-3))))
+        """Rows per call so that one call takes about target_s: a call costs a fixed part (the
+        oracle decodes all of W every call) plus a part per row, measured at 8 and 40 rows."""
+        def secs(n):
+            t0 = time.perf_counter()
+            self.orc.masked_logits(self.Hb, self.rows[:n], self.Wb)
+            return time.perf_counter() - t0
+        t8, t40 = secs(8), secs(40)
+        per_row = max((t40 - t8) / 32, 1e-6)
+        fixed = max(t8 - 8 * per_row, 0.0)
+        self.n = int(max(8, min(len(self.rows), (target_s - fixed) / per_row)))
         return self.n
 
     def run(self):
