@@ -192,8 +192,9 @@ def dist_setup():
 
 
 class CpuOracleTimer:
-    """Times the CPU oracle, as it stands, on a bounded sample of a workload: the first n
-    masked rows of the middle member, all V columns. Inputs are generated once."""
+    """Times the CPU oracle, as it stands, on a bounded sample of a workload: n masked rows of
+    the middle member (its rows in order, repeated cyclically when n exceeds them; repeated
+    indices are valid input), all V columns. Inputs are generated once."""
 
     def __init__(self, ws):
         import numpy as np
@@ -214,27 +215,39 @@ class CpuOracleTimer:
 
     def calibrate(self, target_s):
         """Rows per call so that one call takes about target_s: a call costs a fixed part (the
-        oracle decodes all of W every call) plus a part per row, measured at 8 and 40 rows."""
+        oracle decodes all of W every call) plus a part per row, measured at 256 and 1024 rows
+        (enough rows that the fp64 matmul, not the W stream, sets the per-row cost)."""
+        import numpy as np
+
         def secs(n):
+            rows = np.resize(self.rows, n)
             t0 = time.perf_counter()
-            self.orc.masked_logits(self.Hb, self.rows[:n], self.Wb)
+            self.orc.masked_logits(self.Hb, rows, self.Wb)
             return time.perf_counter() - t0
-        t8, t40 = secs(8), secs(40)
-        per_row = max((t40 - t8) / 32, 1e-6)
-        fixed = max(t8 - 8 * per_row, 0.0)
-        self.n = int(max(8, min(len(self.rows), (target_s - fixed) / per_row)))
+        secs(256)  # first call: pays the one-time costs (allocation, page faults)
+        t_lo, t_hi = secs(256), secs(1024)
+        per_row = max((t_hi - t_lo) / 768, 1e-6)
+        fixed = max(t_lo - 256 * per_row, 0.0)
+        self.n = int(min(8 * len(self.rows), max(256, (target_s - fixed) / per_row)))
         return self.n
 
+    def sample_rows(self):
+        import numpy as np
+
+        return np.resize(self.rows, self.n)
+
     def run(self):
+        rows = self.sample_rows()
         t0 = time.perf_counter()
-        self.orc.masked_logits(self.Hb, self.rows[:self.n], self.Wb)
+        self.orc.masked_logits(self.Hb, rows, self.Wb)
         dt = time.perf_counter() - t0
         flops = 2 * self.n * self.w.V * self.w.d
         return flops / dt / 1e12, dt
 
     def sample(self):
-        return (f"oracle (bf16 decode + fp64 gather and matmul, numpy/OpenBLAS) on the first "
-                f"{self.n} masked rows of {self.w.name}, all V={self.w.V} columns; per call")
+        return (f"oracle (bf16 decode + fp64 gather and matmul, numpy/OpenBLAS) on {self.n} masked "
+                f"rows of {self.w.name} (its {len(self.rows)} rows in order, repeated cyclically), "
+                f"all V={self.w.V} columns; per call")
 
     @staticmethod
     def cpu():
