@@ -129,7 +129,8 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples (every 50 ms, each stamped on arrival) of SM clock and throttle
+    reasons; the summary keeps the samples taken between region_start() and region_end()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -138,24 +139,33 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (monotonic seconds on arrival, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        deadline = time.monotonic() + 3.0  # until the sampler is running (first line)
+        while self.proc and not self.lines and time.monotonic() < deadline:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def region_start(self):
+        self.t0 = time.monotonic()
+
+    def region_end(self):
+        self.t1 = time.monotonic()
 
     def __exit__(self, *a):
         if self.proc:
@@ -168,7 +178,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                continue  # outside the timed region
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 7:
                 continue
@@ -181,7 +193,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample fell inside the timed region"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
 
@@ -196,7 +209,8 @@ def dist_setup():
 class CpuOracleTimer:
     """Times the CPU oracle, as it stands, on a bounded sample of a workload: n masked rows of
     the middle member (its rows in order, repeated cyclically when n exceeds them; repeated
-    indices are valid input), all V columns. Inputs are generated once."""
+    indices are valid input) against all V columns, or against the first cols rows of W when
+    even the smallest row sample would take longer than the target. Inputs are generated once."""
 
     def __init__(self, ws):
         import numpy as np
@@ -214,6 +228,7 @@ class CpuOracleTimer:
         mo = None if mask.mask_offsets is None else mask.mask_offsets.numpy()
         self.rows = orc.resolve_rows(mask.idx.numpy(), w.L_tot, so, mo).astype(np.int32)
         self.n = None
+        self.cols = w.V
 
     def calibrate(self, target_s):
         """Rows per call so that one call takes about target_s: a call costs a fixed part (the
@@ -231,6 +246,11 @@ class CpuOracleTimer:
         per_row = max((t_hi - t_lo) / 768, 1e-6)
         fixed = max(t_lo - 256 * per_row, 0.0)
         self.n = int(min(8 * len(self.rows), max(256, (target_s - fixed) / per_row)))
+        # both parts scale with the columns: fewer of them when 256 rows exceed the target
+        t256 = fixed + 256 * per_row
+        self.cols = self.w.V
+        if target_s < t256:
+            self.cols = max(1024, int(self.w.V * target_s / t256) // 8 * 8)
         return self.n
 
     def sample_rows(self):
@@ -241,15 +261,17 @@ class CpuOracleTimer:
     def run(self):
         rows = self.sample_rows()
         t0 = time.perf_counter()
-        self.orc.masked_logits(self.Hb, rows, self.Wb)
+        self.orc.masked_logits(self.Hb, rows, self.Wb[:self.cols])
         dt = time.perf_counter() - t0
-        flops = 2 * self.n * self.w.V * self.w.d
+        flops = 2 * self.n * self.cols * self.w.d
         return flops / dt / 1e12, dt
 
     def sample(self):
+        cols = (f"all V={self.w.V} columns" if self.cols == self.w.V
+                else f"the first {self.cols} of V={self.w.V} columns")
         return (f"oracle (bf16 decode + fp64 gather and matmul, numpy/OpenBLAS) on {self.n} masked "
                 f"rows of {self.w.name} (its {len(self.rows)} rows in order, repeated cyclically), "
-                f"all V={self.w.V} columns; per call")
+                f"{cols}; per call")
 
     @staticmethod
     def cpu():
@@ -287,7 +309,7 @@ def bench_reference(args):
         v, s = timer.run()
         vals.append(v)
         secs += s
-    value = secs and (2 * timer.n * timer.w.V * timer.w.d * args.steps) / secs / 1e12
+    value = secs and (2 * timer.n * timer.cols * timer.w.d * args.steps) / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -569,6 +591,7 @@ def bench_cuda(args):
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        clk.region_start()
         t_start.record(stream)
         k = 0
         for _ in range(args.steps):
@@ -582,6 +605,7 @@ def bench_cuda(args):
                 k += 1
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.region_end()
     launches = mo.launches - launches0 + (args.steps * captured_launches if graphs else 0)
     if args.mode == "fp8":
         launches += args.steps * len(calls)  # one hidden-state quantization per call
@@ -664,7 +688,7 @@ def bench_cuda(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="llada8b")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
