@@ -75,3 +75,23 @@ def test_reference_arm_non_zero_rank_exits_quietly():
                         "--workload", "tiny", "--steps", "1", "--warmup", "1"],
                        capture_output=True, text=True, timeout=120, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_sampler_keeps_only_the_timed_region():
+    clk = bench.ClockSampler(0)
+    # (arrival time, "sm MHz, max MHz, power, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap")
+    clk.lines = [
+        (0.9, "2070, 2070, 300.0, Not Active, Not Active, Not Active, Not Active"),  # before
+        (1.1, "1600, 2070, 1360.0, Not Active, Not Active, Not Active, Active"),
+        (1.2, "1500, 2070, 1370.0, Not Active, Not Active, Not Active, Active"),
+        (1.3, "1550, 2070, 1365.0, Not Active, Not Active, Not Active, Active"),
+        (1.6, "2070, 2070, 250.0, Active, Not Active, Not Active, Not Active"),       # after
+        (1.25, "garbled line"),
+    ]
+    clk.t0, clk.t1 = 1.0, 1.5
+    s = clk.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1550 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]  # hw_slowdown was seen only outside the region
+    clk.t0, clk.t1 = 5.0, 6.0
+    s = clk.summary()
+    assert s["samples"] == 0 and s["sm_mhz"] is None and "note" in s
