@@ -1,18 +1,25 @@
 """Benchmark of mask-only logits on GB300 (one JSON line on rank 0).
 
-Default workload: the LLaDA-8B-shaped LM head (one sequence L=4096, d=4096, V=126,464, bf16),
-one step = the three mask ratios r_m = 0.1, 0.5, 0.9 computed back to back (M = 410, 2048,
-3686 rows; bf16 logits [M, V]). Inputs are seeded synthetic data resident in HBM; W alone
-(1.04 GB) is larger than L2, so no L2 flush is needed between steps. Each member's public call is
-captured once into a CUDA graph and the timed steps replay it (``--no-graph``: direct calls), so
-host-side argument checks do not leave the GPU idle between the launches of small members.
+Default workload: the Dream-7B-shaped ragged batch, the largest configuration that runs on one GPU:
+8 sequences of L = 32,768 tokens (L_tot = 262,144 hidden rows), d = 3584, V = 152,064, bf16; each
+sequence masks a fraction r_b ~ U(0, 1) of its positions (seeded: M = 172,201 rows in all),
+addressed through per-sequence CSR offsets, and the logits are computed lazily in chunks of 8192
+rows into one reused bf16 output buffer [8192, V] (21 launches per step). One step is one whole
+call. Inputs are seeded synthetic data resident in HBM; W alone (1.09 GB) and every chunk's output
+(2.49 GB) are larger than the 129 MB L2, so no L2 flush is needed between steps. The call is
+captured once into a CUDA graph and the timed steps replay it (``--no-graph``: direct calls).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                  [--mode logits|sample|fp8] [--oracle-timing]
+
+Other workloads (--workload): llada8b (the LLaDA-8B LM head, r_m = 0.1, 0.5, 0.9 back to back),
+decode (16 x 2048 block decode), long (L = 131,072, four mask ratios), tiny, or one member by name.
 
 Under torchrun (N > 1) every rank computes its own batch (different seeds) with no collective
 on the data path; timing is the max over ranks ("weak" scaling).
 ``--impl reference`` times the CPU oracle on this host's cores on a bounded sample of the same
-workload (the comparison arm; rank 0 only).
+workload (the comparison arm; rank 0 only). ``--oracle-timing`` times the oracle on the full
+small configurations and extrapolates it on the large ones (one JSON line per configuration).
 """
 from __future__ import annotations
 
@@ -31,6 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "masked-logits TFLOP/s (and GB/s) at 1 GB300, % of roofline"
 UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "dream"
 
 
 def workload_set(name):
@@ -51,11 +59,12 @@ def workload_set(name):
 def describe(name, ws):
     w0 = ws[0]
     return {
-        "workload": name if len(ws) > 1 else w0.name,
+        "workload": w0.name if len(ws) == 1 else name,
         "members": [w.name for w in ws],
         "B": w0.B, "L": w0.L, "d": w0.d, "V": w0.V,
         "out_dtype": w0.out_dtype,
         "chunk_rows": w0.chunk_rows,
+        "mask": w0.mask_kind,
         "l2": "inputs larger than L2 (W alone exceeds the 129 MB L2); no flush",
     }
 
@@ -65,13 +74,22 @@ def algorithmic_bytes(M, V, d, out_elt):
     return 2 * V * d + 2 * M * d + out_elt * M * V + 4 * M
 
 
+def launch_rows(M, chunk_rows):
+    """Rows of every gather-GEMM launch of one call (one launch per chunk)."""
+    if M == 0:
+        return []
+    if chunk_rows <= 0 or M <= chunk_rows:
+        return [M]
+    return [min(chunk_rows, M - b) for b in range(0, M, chunk_rows)]
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per gather-GEMM launch, from an ncu
 # capture of the kernel sources with the given hash; reported only while the sources still match.
 # Entries: source hash -> {workload: bytes per launch (average over the workload's launches)}.
 MEASURED_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum,
     #     lts__t_sector_hit_rate.pct --clock-control none -k regex:gather_gemm -s 9 -c 3
-    #     python bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
+    #     python bench.py --workload llada8b --no-graph --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
     # r_m 0.1 / 0.5 / 0.9 launches: 1.137 / 1.859 / 2.763 GB (mean per launch below)
     "efb394bd87f06b2b": {"llada8b": 1919696469},
 }
@@ -121,11 +139,41 @@ def sample_bytes(M, V, d, ws_bytes):
 
 
 def load_peaks():
+    """(HBM GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         j = json.load(open(p))
         return j["hbm_gbs"], j["bf16_tflops"], j.get("bf16_tflops_sustained"), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def roofline_entry(tot_flops, tot_bytes, kernel_s, peaks, mode):
+    """The roofline object of the JSON line. The step is timed as a loop of kernel launches of
+    milliseconds each, so the denominator is the burst figure (a kernel timed by itself); the
+    fraction of the sustained figure (cuBLAS looped for seconds under the power cap) is given
+    beside it. E4M3 contractions run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s)."""
+    hbm, bf16, bf16_sus, src = peaks
+    mult = 2 if mode == "fp8" else 1
+    tensor_peak = mult * bf16
+    sus_peak = mult * bf16_sus if bf16_sus else None
+    achieved = tot_flops / kernel_s / 1e12
+    bound = "tensor" if tot_flops / (tensor_peak * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm"
+    src_txt = (f"{src} bf16 dense burst ({'MEASURED_PEAKS.json' if src == 'measured' else 'profiling recipe fallback'})"
+               + (" x 2 (nominal E4M3/bf16 ratio)" if mult == 2 else ""))
+    if bound == "tensor":
+        ach, peak, unit = achieved, tensor_peak, "TFLOP/s"
+    else:
+        ach, peak, unit = tot_bytes / kernel_s / 1e9, hbm, "GB/s"
+    return {
+        "bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+        "peak_source": src_txt,
+        "sustained_peak": sus_peak,
+        "frac_of_sustained_peak": (achieved / sus_peak) if (sus_peak and bound == "tensor") else None,
+        "achieved_tflops": achieved,
+        "achieved_gbs": tot_bytes / kernel_s / 1e9,
+        "hbm_peak_gbs": hbm,
+        "roof_s": max(tot_flops / (tensor_peak * 1e12), tot_bytes / (hbm * 1e9)),
+    }
 
 
 class ClockSampler:
@@ -176,7 +224,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ts, ln in self.lines:
             if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
@@ -189,14 +237,21 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[2]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                     "note": "no nvidia-smi sample fell inside the timed region"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if pw:
+            out["power_w"] = statistics.median(pw)
+        return out
 
 
 def dist_setup():
@@ -210,7 +265,11 @@ class CpuOracleTimer:
     """Times the CPU oracle, as it stands, on a bounded sample of a workload: n masked rows of
     the middle member (its rows in order, repeated cyclically when n exceeds them; repeated
     indices are valid input) against all V columns, or against the first cols rows of W when
-    even the smallest row sample would take longer than the target. Inputs are generated once."""
+    even the smallest row sample would take longer than the target. Inputs are generated once.
+
+    A call costs a fixed part (the oracle decodes all of W on every call) plus a part per row;
+    calibrate() measures both, which also gives the time of a whole step by linear
+    extrapolation in the number of masked rows."""
 
     def __init__(self, ws):
         import numpy as np
@@ -220,6 +279,7 @@ class CpuOracleTimer:
 
         self.orc = orc
         self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        self.ws = ws
         self.w = w = ws[len(ws) // 2]
         mask = w.mask()
         self.Hb = w.hidden("cpu").view(torch.int16).numpy().view(np.uint16)
@@ -229,28 +289,29 @@ class CpuOracleTimer:
         self.rows = orc.resolve_rows(mask.idx.numpy(), w.L_tot, so, mo).astype(np.int32)
         self.n = None
         self.cols = w.V
+        self.fixed = self.per_row = None
 
-    def calibrate(self, target_s):
-        """Rows per call so that one call takes about target_s: a call costs a fixed part (the
-        oracle decodes all of W every call) plus a part per row, measured at 256 and 1024 rows
-        (enough rows that the fp64 matmul, not the W stream, sets the per-row cost)."""
+    def _secs(self, n):
         import numpy as np
 
-        def secs(n):
-            rows = np.resize(self.rows, n)
-            t0 = time.perf_counter()
-            self.orc.masked_logits(self.Hb, rows, self.Wb)
-            return time.perf_counter() - t0
-        secs(256)  # first call: pays the one-time costs (allocation, page faults)
-        t_lo, t_hi = secs(256), secs(1024)
-        per_row = max((t_hi - t_lo) / 768, 1e-6)
-        fixed = max(t_lo - 256 * per_row, 0.0)
-        self.n = int(min(8 * len(self.rows), max(256, (target_s - fixed) / per_row)))
-        # both parts scale with the columns: fewer of them when 256 rows exceed the target
-        t256 = fixed + 256 * per_row
+        rows = np.resize(self.rows, n)
+        t0 = time.perf_counter()
+        self.orc.masked_logits(self.Hb, rows, self.Wb)
+        return time.perf_counter() - t0
+
+    def calibrate(self, target_s, lo=256, hi=1024):
+        """Rows per call so that one call takes about target_s (measured at lo and hi rows:
+        enough rows that the fp64 matmul, not the W stream, sets the per-row cost)."""
+        self._secs(lo)  # first call: pays the one-time costs (allocation, page faults)
+        t_lo, t_hi = self._secs(lo), self._secs(hi)
+        self.per_row = max((t_hi - t_lo) / (hi - lo), 1e-7)
+        self.fixed = max(t_lo - lo * self.per_row, 0.0)
+        self.n = int(min(8 * len(self.rows), max(lo, (target_s - self.fixed) / self.per_row)))
+        # both parts scale with the columns: fewer of them when lo rows exceed the target
+        t_lo_est = self.fixed + lo * self.per_row
         self.cols = self.w.V
-        if target_s < t256:
-            self.cols = max(1024, int(self.w.V * target_s / t256) // 8 * 8)
+        if target_s < t_lo_est:
+            self.cols = max(1024, int(self.w.V * target_s / t_lo_est) // 8 * 8)
         return self.n
 
     def sample_rows(self):
@@ -265,6 +326,11 @@ class CpuOracleTimer:
         dt = time.perf_counter() - t0
         flops = 2 * self.n * self.cols * self.w.d
         return flops / dt / 1e12, dt
+
+    def step_seconds(self, Ms):
+        """Whole-step oracle time, extrapolated linearly in the masked rows: one call per member
+        (the fixed W decode each time) plus the per-row cost of every row."""
+        return sum(self.fixed + self.per_row * M for M in Ms)
 
     def sample(self):
         cols = (f"all V={self.w.V} columns" if self.cols == self.w.V
@@ -292,6 +358,35 @@ class CpuOracleTimer:
         except OSError:
             pass
         return f"{platform.machine()}, {model or 'model unknown'}, {os.cpu_count()} logical cores"
+
+
+def oracle_probe(workload, target_s):
+    """Child-process entry of the single-thread oracle figure: the process was started with one
+    BLAS / OpenMP thread; prints {tflops, seconds, n, cols, fixed_s, per_row_s} as JSON."""
+    ws = workload_set(workload)
+    t = CpuOracleTimer(ws)
+    t.calibrate(target_s, lo=16, hi=64)
+    v, secs = t.run()
+    print(json.dumps({"tflops": v, "seconds": secs, "n": t.n, "cols": t.cols,
+                      "fixed_s": t.fixed, "per_row_s": t.per_row, "sample": t.sample()}))
+
+
+def single_thread_oracle(workload, target_s, Ms):
+    """The oracle on one host core (a child process with one BLAS thread): its rate on a sample
+    and the whole step's time extrapolated from it. None if the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    env.pop("RANK", None), env.pop("WORLD_SIZE", None), env.pop("LOCAL_RANK", None)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-probe",
+                            "--workload", workload, "--ref-step-s", str(target_s)],
+                           capture_output=True, text=True, timeout=600, env=env)
+        j = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+    step = sum(j["fixed_s"] + j["per_row_s"] * M for M in Ms)
+    return {"value": j["tflops"], "unit": UNIT, "cores": 1, "seconds": j["seconds"],
+            "sample": j["sample"],
+            "step_s_extrapolated": step}
 
 
 def bench_reference(args):
@@ -324,13 +419,53 @@ def bench_reference(args):
     return 0
 
 
+def oracle_timing(args):
+    """The oracle's time for whole configurations on this host's cores: measured on the ones it
+    finishes in seconds (Tiny, the LLaDA-8B ratios, block decode), extrapolated linearly in the
+    masked rows (fixed W decode per call plus a per-row cost, both measured) on the long-context
+    and Dream-shaped ones. One JSON line per configuration."""
+    import numpy as np
+
+    from masked_token_lm_gb300 import workloads as wl
+    from oracle import mask_only_logits as orc
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for w in [wl.TINY] + wl.LLADA + [wl.DECODE] + wl.LONG + [wl.DREAM]:
+        import torch
+
+        mask = w.mask()
+        flops = w.flops(mask.M)
+        if w in wl.LONG or w is wl.DREAM:
+            t = CpuOracleTimer([w])
+            t.calibrate(args.ref_step_s)
+            secs, how = t.step_seconds([mask.M]), "extrapolated"
+        else:
+            Hb = w.hidden("cpu").view(torch.int16).numpy().view(np.uint16)
+            Wb = w.weight("cpu").view(torch.int16).numpy().view(np.uint16)
+            so = None if mask.seq_offsets is None else mask.seq_offsets.numpy()
+            mo = None if mask.mask_offsets is None else mask.mask_offsets.numpy()
+            rows = orc.resolve_rows(mask.idx.numpy(), w.L_tot, so, mo)
+            orc.masked_logits(Hb, rows[:8], Wb)  # warm-up: one-time allocation and page faults
+            t0 = time.perf_counter()
+            orc.masked_logits(Hb, mask.idx.numpy(), Wb, so, mo)
+            secs, how = time.perf_counter() - t0, "measured"
+        print(json.dumps({"workload": w.name, "M": mask.M, "flop": flops, "oracle_s": secs,
+                          "tflops": flops / secs / 1e12, "how": how, "cores": cores,
+                          "cpu": CpuOracleTimer.cpu()}), flush=True)
+    return 0
+
+
 def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     """The same step end to end through the public call: every step copies its inputs (H, idx,
     CSR offsets and W) from pinned host memory to the device and reads all logits back to pinned
     host memory. Uploads and read-backs run on their own streams and overlap compute and each
-    other (within and across steps); W has two device buffers, used by alternate steps, so one
-    step's W upload does not wait for the previous step's last member. The timed region spans all
-    of it."""
+    other (within and across steps); W and H have two device buffers each, used by alternate
+    steps, so one step's uploads do not wait for the previous step's compute. Unchunked members
+    read their [M, V] logits back into a pinned [M, V] host buffer. Chunked members read every
+    chunk back into one reused pinned [chunk_rows, V] host buffer: the chunk callback (the
+    consumer) copies the chunk out of the library's buffer into one of two device staging
+    buffers on the compute stream, so the next chunk can start while the read-back runs. The
+    timed region spans all of it."""
     import torch
 
     host_in, host_out = [], []
@@ -345,66 +480,74 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
                 hi[k2] = t.cpu().pin_memory()
         host_in.append(hi)
         h2d += sum(t.numel() * t.element_size() for t in hi.values())
-        ho = torch.empty((c["mask"].M, c["w"].V), dtype=c["odt"], pin_memory=True)
+        rows_host = c["w"].chunk_rows if c["chunked"] else c["mask"].M
+        ho = torch.empty((rows_host, c["w"].V), dtype=c["odt"], pin_memory=True)
         host_out.append(ho)
-        d2h += ho.numel() * ho.element_size()
-    dev_in = [{k2: torch.empty_like(v, device=dev) for k2, v in hi.items() if k2 != "W"}
-              for hi in host_in]
-    dev_w = [[torch.empty_like(hi["W"], device=dev) if "W" in hi else None for hi in host_in]
-             for _ in range(2)]
-    # one device output buffer per member so read-backs can overlap the next member's compute
+        d2h += c["mask"].M * c["w"].V * ho.element_size()
+    # two sets of device inputs, used by alternate steps
+    dev_in = [[{k2: torch.empty_like(v, device=dev) for k2, v in hi.items()} for hi in host_in]
+              for _ in range(2)]
     dev_out = [torch.empty_like(c["out"]) for c in calls]
+    staging = [[torch.empty_like(c["out"]) for _ in range(2)] if c["chunked"] else None
+               for c in calls]
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
 
-    # Ordering per member: its inputs may be overwritten once its compute has consumed them,
-    # its output buffer once its read-back is done. Nothing else is serialised, so uploads of
-    # step k+1 overlap read-backs of step k (opposite directions, separate copy engines).
-    consumed = [None] * len(calls)
-    w_consumed = [None, None]  # last use of each W buffer (the last member of its step)
-    read_back = [None] * len(calls)
+    consumed = [[None] * len(calls) for _ in range(2)]  # last use of each input set per member
+    read_back = [None] * len(calls)                     # read-back of each member's output done
+    stage_free = [[None, None] for _ in calls]          # read-back of each staging buffer done
     parity = [0]
 
     def e2e_step():
+        par = parity[0]
         Wd = None
-        wb = dev_w[parity[0]]
-        for j, (c, hi, di, ho, do) in enumerate(zip(calls, host_in, dev_in, host_out, dev_out)):
+        for j, (c, hi, ho, do) in enumerate(zip(calls, host_in, host_out, dev_out)):
+            di = dev_in[par][j]
             with torch.cuda.stream(s_in):
-                if "W" in hi:
-                    if w_consumed[parity[0]] is not None:
-                        s_in.wait_event(w_consumed[parity[0]])
-                    wb[j].copy_(hi["W"], non_blocking=True)
-                if consumed[j] is not None:
-                    s_in.wait_event(consumed[j])
+                if consumed[par][j] is not None:
+                    s_in.wait_event(consumed[par][j])
+                if j == 0 and consumed[par][-1] is not None:
+                    # member 0's W buffer serves every member of the step: wait for the last one
+                    s_in.wait_event(consumed[par][-1])
                 for k2, v in hi.items():
-                    if k2 != "W":
-                        di[k2].copy_(v, non_blocking=True)
+                    di[k2].copy_(v, non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(s_in)
             stream.wait_event(ready)
-            if read_back[j] is not None:
+            if read_back[j] is not None and not c["chunked"]:
                 stream.wait_event(read_back[j])
-            Wd = wb[j] if "W" in hi else Wd
+            Wd = di["W"] if "W" in di else dev_in[par][0]["W"]
 
-            def on_chunk(ci, rb, rows, out, ho=ho, c=c):
-                done = torch.cuda.Event()
-                done.record(stream)
+            def on_chunk(ci, rb, rows, out, j=j, ho=ho, c=c):
+                if not c["chunked"]:
+                    done = torch.cuda.Event()
+                    done.record(stream)
+                    s_out.wait_event(done)
+                    with torch.cuda.stream(s_out):
+                        ho.copy_(out, non_blocking=True)
+                    return
+                k = ci % 2
+                st = staging[j][k]
+                with torch.cuda.stream(stream):
+                    if stage_free[j][k] is not None:
+                        stream.wait_event(stage_free[j][k])
+                    st[:rows].copy_(out[:rows], non_blocking=True)
+                    done = torch.cuda.Event()
+                    done.record(stream)
                 s_out.wait_event(done)
                 with torch.cuda.stream(s_out):
-                    ho[rb:rb + rows].copy_(out[:rows], non_blocking=True)
-                if c["chunked"]:  # the next chunk reuses `out`: wait for its read-back
-                    drained = torch.cuda.Event()
-                    drained.record(s_out)
-                    stream.wait_event(drained)
+                    ho[:rows].copy_(st[:rows], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_out)
+                stage_free[j][k] = ev
 
             mo.masked_logits(di["H"], di["idx"], Wd, di.get("so"), di.get("mo"), out=do,
                              chunk_rows=c["w"].chunk_rows, on_chunk=on_chunk, stream=stream)
-            consumed[j] = torch.cuda.Event()
-            consumed[j].record(stream)
+            ev_c = torch.cuda.Event()
+            ev_c.record(stream)
+            consumed[par][j] = ev_c
             read_back[j] = torch.cuda.Event()
             read_back[j].record(s_out)
-        # this step's W buffer is used by every member: not overwritten before the last is done
-        w_consumed[parity[0]] = consumed[-1]
         parity[0] ^= 1
 
     for _ in range(max(1, args.warmup)):
@@ -429,13 +572,18 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
         raise SystemExit(f"kernel status in the e2e leg: {mz.mosaic_last_error_string()}")
     return {"value": world * tot_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-            "steps": n_e2e, "path": "pinned host -> Mosaic.masked_logits -> pinned host"}
+            "steps": n_e2e,
+            "path": "pinned host -> Mosaic.masked_logits (C ABI) -> pinned host; chunks read back "
+                    "through two device staging buffers into one reused pinned chunk buffer"}
 
 
-def bench_cublas_context(args, calls, tot_flops, stream):
+def cublas_context(args, calls, replay_step, tot_flops, stream, local):
     """Context only (not a target, not this library): the same step done unfused by torch --
     index_select of the masked rows into a gathered buffer, then a cuBLAS bf16 matmul with W^T
-    (flat index lists; CSR members use their resolved rows)."""
+    into the same output buffer, chunk by chunk as the library's call is chunked (CSR members use
+    their resolved rows). It runs interleaved step by step with this library's step (A/B/A/B,
+    the same step count, after the same warm-up) inside one clock-sampled region, so both see the
+    same clocks; per-step CUDA events time each side."""
     import torch
 
     prepared = []
@@ -447,26 +595,44 @@ def bench_cublas_context(args, calls, tot_flops, stream):
             counts = (m.mask_offsets[1:] - m.mask_offsets[:-1]).long()
             seq = torch.repeat_interleave(torch.arange(counts.numel(), device=counts.device), counts)
             rows = m.seq_offsets.long()[seq] + m.idx.long()
-        prepared.append((c, rows))
+        cr = c["out"].shape[0]
+        gbuf = torch.empty((cr, c["w"].d), dtype=torch.bfloat16, device=c["H"].device)
+        out = torch.empty_like(c["out"])
+        prepared.append((c, rows, gbuf, out, launch_rows(m.M, c["w"].chunk_rows)))
 
-    def step():
-        for c, rows in prepared:
-            a = torch.index_select(c["H"], 0, rows)
-            torch.matmul(a, c["W"].t())
+    def cublas_step():
+        for c, rows, gbuf, out, chunks in prepared:
+            rb = 0
+            for n in chunks:
+                torch.index_select(c["H"], 0, rows[rb:rb + n], out=gbuf[:n])
+                torch.matmul(gbuf[:n], c["W"].t(), out=out[:n])
+                rb += n
 
     for _ in range(args.warmup):
-        step()
+        cublas_step()
+        replay_step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(1, min(args.steps, 10))
-    e0.record(stream)
-    for _ in range(n):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / n
-    return {"value": tot_flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
-            "what": "torch index_select + cuBLAS bf16 matmul (unfused, writes the gathered rows)"}
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    with ClockSampler(local) as clk:
+        clk.region_start()
+        for s in range(n):
+            ev[s][0].record(stream)
+            replay_step()
+            ev[s][1].record(stream)
+            ev[s][2].record(stream)
+            cublas_step()
+            ev[s][3].record(stream)
+        torch.cuda.synchronize()
+        clk.region_end()
+    fused_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    cub_ms = sum(e[2].elapsed_time(e[3]) for e in ev) / n
+    return {"value": tot_flops / (cub_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": cub_ms,
+            "fused_ms_per_step_same_region": fused_ms,
+            "fused_over_cublas_speed": cub_ms / fused_ms,
+            "steps": n, "clocks": clk.summary(),
+            "what": "torch index_select + cuBLAS bf16 matmul per chunk (unfused, writes the "
+                    "gathered rows), interleaved A/B with this library's step"}
 
 
 def bench_cuda(args):
@@ -492,6 +658,7 @@ def bench_cuda(args):
     seed_shift = rank_seed_shift(rank)
     calls = []
     tot_flops = tot_bytes = 0
+    n_launch_units = 0  # gather-GEMM launches per step
     for w in ws:
         mask = w.mask().to(dev)
         H = wl.make_hidden(w.L_tot, w.d, w.seed + 1 + seed_shift, dev)
@@ -513,6 +680,7 @@ def bench_cuda(args):
             tot_bytes += algorithmic_bytes(mask.M, w.V, w.d, out.element_size())
         calls.append(call)
         tot_flops += w.flops(mask.M)
+        n_launch_units += len(launch_rows(mask.M, w.chunk_rows))
     # identical W across members of one workload set: share it
     for c in calls[1:]:
         if c["w"].V == calls[0]["w"].V and c["w"].d == calls[0]["w"].d:
@@ -581,6 +749,16 @@ def bench_cuda(args):
             g.replay()
         torch.cuda.synchronize()
 
+    def replay_member(j):
+        if graphs:
+            graphs[j].replay()
+        else:
+            one_call(calls[j])
+
+    def replay_step():
+        for j in range(len(calls)):
+            replay_member(j)
+
     # ---- device-timed region: per-call events on the launching stream
     if world > 1:
         torch.distributed.barrier()
@@ -595,12 +773,9 @@ def bench_cuda(args):
         t_start.record(stream)
         k = 0
         for _ in range(args.steps):
-            for j, c in enumerate(calls):
+            for j in range(len(calls)):
                 evs[k][0].record(stream)
-                if graphs:
-                    graphs[j].replay()
-                else:
-                    one_call(c)
+                replay_member(j)
                 evs[k][1].record(stream)
                 k += 1
         t_end.record(stream)
@@ -629,20 +804,28 @@ def bench_cuda(args):
 
     cublas = None
     if not args.no_cublas_context and args.mode == "logits":
-        cublas = bench_cublas_context(args, calls, tot_flops, stream)
+        cublas = cublas_context(args, calls, replay_step, tot_flops, stream, local)
 
-    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    peaks = load_peaks()
     clocks = clk.summary()
-    # The peak of the clock regime the timed region ran in: the sustained bf16 figure (measured
-    # back to back for seconds, under the power cap) when the power cap was active during the
-    # region, else the burst figure. The contraction's own peak: E4M3 runs at twice the bf16 rate
-    # (nominal 4.5 vs 2.25 PFLOP/s).
-    capped = "sw_power_cap" in clocks["reasons"] and bf16_sus is not None
-    bf16_peak = bf16_sus if capped else bf16
-    tensor_peak = 2 * bf16_peak if args.mode == "fp8" else bf16_peak
-    burst_peak = 2 * bf16 if args.mode == "fp8" else bf16
-    kernel_tflops = tot_flops * args.steps / (kernel_ms * 1e-3) / 1e12
-    roof_time = max(tot_flops / (tensor_peak * 1e12), tot_bytes / (hbm * 1e9))
+    roof = roofline_entry(tot_flops * args.steps, tot_bytes * args.steps, kernel_ms * 1e-3,
+                          peaks, args.mode)
+    traffic = None
+    if args.traffic is not None:
+        traffic = args.traffic
+    elif args.mode == "logits":
+        traffic = MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(args.workload)
+    roof.update({
+        "traffic": traffic,
+        "traffic_per": "launch (mean over the step's gather-GEMM launches)",
+        "launches_per_step": n_launch_units,
+        "algorithmic_bytes_per_launch": tot_bytes / max(1, n_launch_units),
+        "kernel": ("gather_gemm_kernel<fp8> + per-step masked-row quantization"
+                   if args.mode == "fp8" else
+                   "gather_gemm_kernel<sample> + sample_reduce_kernel" if args.mode == "sample"
+                   else "gather_gemm_kernel<bf16 out, CTA pair>"),
+        "timing": "CUDA events around every member call on the launching stream, summed",
+    })
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -650,6 +833,8 @@ def bench_cuda(args):
         "dtype": "e4m3" if args.mode == "fp8" else "bf16", "data": "synthetic",
         "config": {**describe(args.workload, ws),
                    "M": [c["mask"].M for c in calls],
+                   "flop_per_step": tot_flops,
+                   "algorithmic_bytes_per_step": tot_bytes,
                    "parallelism": f"replicas x{world} (independent batches, no collective)",
                    "launch": "direct calls" if args.no_graph else
                              "one CUDA-graph replay per member call (captured from the public calls)"},
@@ -657,26 +842,7 @@ def bench_cuda(args):
         "member_ms": dict(zip([c["w"].name for c in calls], member_ms)),
         "mode": args.mode,
         "kernel_source_hash": kernel_source_hash(),
-        "roofline_frac_of_step": roof_time / (ms_per_step * 1e-3) if world == 1 else None,
-        "roofline": {
-            "bound": "tensor" if tot_flops / (tensor_peak * 1e12) >= tot_bytes / (hbm * 1e9) else "hbm",
-            "achieved": kernel_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
-            "frac": kernel_tflops / tensor_peak,
-            "frac_of_burst_peak": kernel_tflops / burst_peak,
-            "traffic": (args.traffic if args.traffic is not None
-                        else MEASURED_TRAFFIC.get(kernel_source_hash(), {}).get(args.workload)
-                        if args.mode == "logits" else None),
-            "peak_source": ((f"{peak_src} bf16 dense "
-                             + ("sustained (sw_power_cap was active in the timed region)" if capped
-                                else "burst") + " (MEASURED_PEAKS.json)")
-                            if peak_src == "measured" else
-                            "fallback " + ("1.7 PFLOP/s sustained" if capped else "1.9 PFLOP/s burst"))
-                           + (" x 2 (nominal E4M3/bf16 ratio)" if args.mode == "fp8" else ""),
-            "kernel": ("gather_gemm_kernel<fp8> + per-step masked-row quantization"
-                       if args.mode == "fp8" else "gather_gemm_kernel<false>"),
-            "achieved_gbs": tot_bytes * args.steps / (kernel_ms * 1e-3) / 1e9,
-            "hbm_peak_gbs": hbm,
-        },
+        "roofline": roof,
         "gpu_launches": launches,
         "cublas_context": cublas,
         "clocks": clocks,
@@ -686,8 +852,15 @@ def bench_cuda(args):
         timer = CpuOracleTimer(ws)
         timer.calibrate(args.ref_step_s)
         v, secs = timer.run()
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
-                                "sample": timer.sample(), "seconds": secs, "cpu": timer.cpu()}
+        Ms = [c["mask"].M for c in calls]
+        line["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": timer.cores, "kind": "oracle",
+            "sample": timer.sample(), "seconds": secs, "cpu": timer.cpu(),
+            "step_s_extrapolated": timer.step_seconds(Ms),
+            "step_extrapolation": "whole step, linear in the masked rows: one W decode per call "
+                                  "plus the measured per-row cost",
+            "single_thread": single_thread_oracle(args.workload, args.ref_step_s_single, Ms),
+        }
     if rank == 0:
         print(json.dumps(line), flush=True)
     mo.close()
@@ -699,9 +872,9 @@ def bench_cuda(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="llada8b")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--mode", default="logits", choices=["logits", "sample", "fp8"],
                     help="logits: [M, V] mask-only logits (the metric); sample: fused greedy "
@@ -714,9 +887,19 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct calls instead of one CUDA-graph replay per member call")
     ap.add_argument("--ref-step-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s-single", type=float, default=8.0,
+                    help="target seconds of the single-thread oracle sample")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of the current kernel")
+    ap.add_argument("--oracle-timing", action="store_true",
+                    help="time the oracle on whole configurations (no GPU)")
+    ap.add_argument("--oracle-probe", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_probe:
+        oracle_probe(args.workload, args.ref_step_s)
+        return 0
+    if args.oracle_timing:
+        return oracle_timing(args)
     if args.warmup < 3 and args.impl == "cuda":
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

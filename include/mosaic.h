@@ -286,13 +286,19 @@ MOSAIC_API const char* mosaic_last_error_string(void);
  * anything is enqueued. Every GPU that loads the library holds that array until exit.
  *
  * chunk_status   optional HOST array of at least that many uint32 words. NULL: the call is
- *                asynchronous and reports only argument errors. Non-NULL: the call waits for
- *                `stream`, copies each chunk's status word there (bit 1: a bad mask index or
- *                CSR offsets, bit 2: a bounded wait ran out) and returns MOSAIC_ERR_INDEX /
- *                MOSAIC_ERR_TIMEOUT / MOSAIC_OK accordingly.
+ *                asynchronous and reports only argument errors; a bad mask index then yields a
+ *                zero-filled output row that nothing reports, so pass the array at least while
+ *                debugging. Non-NULL: the call waits for `stream`, copies each chunk's status
+ *                word there (bit 1: a bad mask index or CSR offsets, bit 2: a bounded wait ran
+ *                out) and returns MOSAIC_ERR_INDEX / MOSAIC_ERR_TIMEOUT / MOSAIC_OK accordingly.
+ *
+ * Every wait inside the kernel gives up after a fixed 2 seconds (there is no handle, so
+ * mosaic_set_wait_timeout does not apply here).
  *
  * The first call on a device sets that device up (kernel attributes, occupancy, the array's
- * device address); make it before any CUDA stream capture. All calls share the one array,
+ * device address, kept until the process exits); make it before any CUDA stream capture, and do
+ * not call this entry point on a device after cudaDeviceReset() of that device (the library's
+ * device code is loaded again and the kept address would be stale). All calls share the one array,
  * which keeps the last call's words: each call clears the words it uses on `stream` before
  * its kernels run, so calls that overlap on the GPU (different streams, no ordering) race
  * on the status words and their reported status is unreliable; the logits are unaffected.

@@ -100,11 +100,17 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t elt, const void* b
   return r == CUDA_SUCCESS;
 }
 
+// L2 bytes a raster group's gathered rows may take (compile-time, for tuning runs).
+#ifndef MOSAIC_L2_GROUP_BYTES
+#define MOSAIC_L2_GROUP_BYTES (64ll << 20)
+#endif
+
 // M units per raster group: as many as keep the group's gathered rows (cluster_m x BM rows of
-// row_bytes per unit) within ~64 MiB of L2, so that W panels are streamed once per group.
+// row_bytes per unit) within MOSAIC_L2_GROUP_BYTES of L2, so that W panels are streamed once per
+// group.
 int pick_group_u(int m_units, int cm, int64_t row_bytes) {
   const int64_t per_unit = static_cast<int64_t>(cm) * mosaic::gather_gemm_block_m() * row_bytes;
-  int64_t g = (64ll << 20) / per_unit;
+  int64_t g = static_cast<int64_t>(MOSAIC_L2_GROUP_BYTES) / per_unit;
   if (g < 1) g = 1;
   if (g > m_units) g = m_units;
   return static_cast<int>(g);

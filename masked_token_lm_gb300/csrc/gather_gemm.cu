@@ -618,39 +618,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
         const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
         if constexpr (SAMPLE) {
-          // Sampling epilogue: this row's running max, first argmax and sum of exp(x - max) over
-          // the half's valid columns (fp32 logits straight from TMEM), merged chunk by chunk;
-          // then the two halves of the row are merged through shared memory.
+          // Sampling epilogue: this row's maximum, its first column and the sum of exp(x - max)
+          // over the half's valid columns (fp32 logits straight from TMEM), in two blocks of 64
+          // columns; the slot is handed back right after the second block's TMEM read, before
+          // its arithmetic. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per
+          // column. Columns past V are checked for only where a block reaches past V. The two
+          // halves of the row are then merged through shared memory.
+          constexpr float LOG2E = 1.4426950408889634f;
           float m = -INFINITY, s = 0.0f;
           int a = 0;
-          for (int c = 0; c < BN / 2 / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_acc + c * 32, v);
+          const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
+          uint32_t v[64];
+          auto load64 = [&](int c0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tmem_ld_32x32b_x16(t_acc + c0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(v + q * 16));
             tmem_wait_ld();
-            const int col0 = n0 + c * 32;
-            float cm = -INFINITY;
-            int ca = 0;
+          };
+          auto block = [&](int c0) {
+            const bool inside = valid >= c0 + 64;
+            float bm = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = __uint_as_float(v[j]);
-              if (col0 + j < p.V && x > cm) { cm = x; ca = col0 + j; }
+            for (int j = 0; j < 64; ++j)
+              if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[j]));
+            if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
+              int ba = 0;
+#pragma unroll
+              for (int j = 63; j >= 0; --j)
+                if (__uint_as_float(v[j]) == bm && (inside || c0 + j < valid)) ba = j;
+              s *= ex2_approx((m - bm) * LOG2E);
+              m = bm;
+              a = n0 + c0 + ba;
             }
-            if (cm > m) { s *= __expf(m - cm); m = cm; a = ca; }
+            const float mL = m * LOG2E;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V) s += __expf(__uint_as_float(v[j]) - m);
-          }
+            for (int j = 0; j < 64; ++j)
+              if (inside || c0 + j < valid) s += ex2_approx(fmaf(__uint_as_float(v[j]), LOG2E, -mL));
+          };
+          load64(0);
+          block(0);
+          load64(64);
+          release_slot(slot);
+          block(64);
           float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);
           float* xs = xm + BM;
           int* xa = reinterpret_cast<int*>(xs + BM);
           if (half == 1) { xm[row_in_tile] = m; xs[row_in_tile] = s; xa[row_in_tile] = a; }
-          release_slot(slot);  // also orders the exchange above before the reads below
+          named_bar_sync(1, EPI_THREADS);  // the exchange above before the reads below
           if (half == 0) {
             const float m1 = xm[row_in_tile], s1 = xs[row_in_tile];
             const int a1 = xa[row_in_tile];
             // columns of half 0 come first: an equal maximum keeps half 0's index
-            if (m1 > m) { s = s * __expf(m - m1) + s1; m = m1; a = a1; }
-            else if (s1 > 0.0f) { s += s1 * __expf(m1 - m); }
+            if (m1 > m) { s = s * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
+            else if (s1 > 0.0f) { s += s1 * ex2_approx((m1 - m) * LOG2E); }
             if (r < p.rows && tc.m < p.m_tiles) {
               const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
               p.part_max[o] = m;

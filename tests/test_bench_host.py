@@ -95,3 +95,26 @@ def test_clock_sampler_keeps_only_the_timed_region():
     clk.t0, clk.t1 = 5.0, 6.0
     s = clk.summary()
     assert s["samples"] == 0 and s["sm_mhz"] is None and "note" in s
+
+
+def test_launch_rows_follow_the_chunking_rule():
+    assert bench.launch_rows(0, 4096) == []
+    assert bench.launch_rows(100, 0) == [100]
+    assert bench.launch_rows(100, 100) == [100]
+    assert bench.launch_rows(172201, 8192) == [8192] * 21 + [169]
+
+
+def test_roofline_uses_the_burst_peak_and_reports_the_sustained_fraction():
+    peaks = (6784.8, 1898.6, 1685.2, "measured")
+    flops, nbytes = 2 * 2048 * 126464 * 4096, bench.algorithmic_bytes(2048, 126464, 4096, 2)
+    r = bench.roofline_entry(flops, nbytes, 1.2e-3, peaks, "logits")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1898.6
+    assert abs(r["achieved"] - flops / 1.2e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / 1898.6) < 1e-12
+    assert abs(r["frac_of_sustained_peak"] - r["achieved"] / 1685.2) < 1e-12
+    r8 = bench.roofline_entry(flops, nbytes, 1.2e-3, peaks, "fp8")
+    assert r8["peak"] == 2 * 1898.6 and "E4M3" in r8["peak_source"]
+    # far below the ridge the HBM roof binds and the fraction is of bandwidth
+    small = bench.roofline_entry(2 * 16 * 126464 * 4096, bench.algorithmic_bytes(16, 126464, 4096, 2),
+                                 1.8e-4, peaks, "logits")
+    assert small["bound"] == "hbm" and small["unit"] == "GB/s" and small["peak"] == 6784.8

@@ -171,3 +171,38 @@ def test_fp8_argument_errors():
     x = torch.zeros((4, 24), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(mz.MosaicError):
         mz.quantize_rows_e4m3(x)                      # d % 16 != 0
+
+
+@pytest.mark.parametrize("csr", [False, True])
+def test_fp8_whole_chain_against_the_oracle_from_bf16_inputs(mo, csr):
+    """The expected side is all oracle: it quantizes the bf16 inputs itself (rows of H and W)
+    and computes the quantized logits; the GPU side runs its own quantization kernels and the
+    FP8 logits. No GPU-produced value enters the expected side."""
+    d, V = 512, 1544
+    if csr:
+        m = wl.ragged_mask(3, 400, seed=31)
+        L = 1200
+        so, mo_ = m.seq_offsets, m.mask_offsets
+        idx = m.idx
+    else:
+        L = 900
+        idx = wl.uniform_positions(L, 333, seed=32)
+        so = mo_ = None
+    H = wl.make_hidden(L, d, 33, DEV)
+    W = wl.make_weight(V, d, 34, DEV)
+    # oracle: quantize from the bf16 bit patterns, then the FP8 logits
+    qH_ref, sH_ref = f8.quantize_rows(bits(H))
+    qW_ref, sW_ref = f8.quantize_rows(bits(W))
+    ref = f8.masked_logits_fp8(qH_ref, sH_ref, idx.numpy(), qW_ref, sW_ref,
+                               None if so is None else so.numpy(),
+                               None if mo_ is None else mo_.numpy())
+    # GPU: W quantized once, the masked hidden rows quantized, then the fused FP8 logits
+    qW, sW = mz.quantize_rows_e4m3(W)
+    qH = torch.zeros((L, d), dtype=torch.uint8, device=DEV)
+    sH = torch.zeros((L,), dtype=torch.float32, device=DEV)
+    dev = lambda t: None if t is None else t.to(DEV)  # noqa: E731
+    mz.quantize_masked_rows_e4m3(H, idx.to(DEV), qH, sH, dev(so), dev(mo_))
+    for dt in (torch.bfloat16, torch.float32):
+        out = mo.masked_logits_fp8(qH, sH, idx.to(DEV), qW, sW, dev(so), dev(mo_), out_dtype=dt)
+        assert mo.check() == mz.MOSAIC_OK
+        assert_close(out, ref, dt, f"whole FP8 chain, csr={csr}, {dt}")

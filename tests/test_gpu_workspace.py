@@ -5,6 +5,8 @@ import torch
 
 from masked_token_lm_gb300 import mosaic as mz
 from masked_token_lm_gb300 import workloads as wl
+from oracle import mask_only_logits as orc
+from tests.parity_utils import assert_close, bits
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -38,6 +40,10 @@ def test_workspace_as_lazy_chunk_output_matches_plain_buffer():
     idx = wl.uniform_positions(L, M, seed=63).to(DEV)
     mo = mz.Mosaic(0)
     ref = mo.masked_logits(H, idx, W, out_dtype=torch.bfloat16)
+    assert mo.check() == mz.MOSAIC_OK
+    # the plain-buffer result itself against the oracle (fp64), every element
+    exact = orc.masked_logits(bits(H), idx.cpu().numpy(), bits(W))
+    assert_close(ref, exact, torch.bfloat16, "plain buffer vs oracle")
     ws = mz.Workspace(M * V * 2)  # reserved for the unchunked output, bound per chunk size
     try:
         full = torch.empty((M, V), dtype=torch.bfloat16, device=DEV)
@@ -51,6 +57,7 @@ def test_workspace_as_lazy_chunk_output_matches_plain_buffer():
             mo.masked_logits(H, idx, W, out=out, chunk_rows=chunk_rows, on_chunk=on_chunk)
             assert mo.check() == mz.MOSAIC_OK
             assert torch.equal(full.view(torch.int16), ref.view(torch.int16))
+            assert_close(full, exact, torch.bfloat16, f"workspace chunks of {chunk_rows} vs oracle")
     finally:
         torch.cuda.synchronize()
         del out

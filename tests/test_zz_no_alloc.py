@@ -87,3 +87,47 @@ def test_noalloc_chunked_status_per_chunk_and_limit():
     st = _noalloc(H, many, W, out, chunk_rows=1, cb=cb)
     assert st == mz.MOSAIC_ERR_UNSUPPORTED
     assert "status words" in mz.mosaic_last_error_string()
+
+
+def test_noalloc_csr_chunked_matches_handle_and_reports_bad_offsets():
+    """A CSR batch of three sequences, one of them empty, cut into chunks that cross sequence
+    boundaries: bit for bit the handle entry point's result. Then mask_offsets that do not end at
+    M: the kernel's offsets check (made by the first chunk's launch) sets chunk 0's word only."""
+    torch.cuda.set_device(0)
+    d, V, L = 512, 1032, 500
+    so = torch.tensor([0, 500, 500, 1000], dtype=torch.int32)     # sequence 1 is empty
+    a = wl.uniform_positions(L, 300, 91)
+    b = wl.uniform_positions(L, 250, 92)
+    idx = torch.cat([a, b])
+    M = idx.numel()
+    moff = torch.tensor([0, 300, 300, M], dtype=torch.int32)
+    H = wl.make_hidden(1000, d, 93, DEV)
+    W = wl.make_weight(V, d, 94, DEV)
+    idx, so, moff = idx.to(DEV), so.to(DEV), moff.to(DEV)
+    mo = mz.Mosaic(0)
+    ref = mo.masked_logits(H, idx, W, so, moff, out_dtype=torch.bfloat16)
+    assert mo.check() == mz.MOSAIC_OK
+    mo.close()
+    chunk = 256
+    n_chunks = (M + chunk - 1) // chunk
+    full = torch.empty((M, V), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((chunk, V), dtype=torch.bfloat16, device=DEV)
+
+    def on_chunk(c, rb, rows, ptr, user):
+        full[rb:rb + rows].copy_(out[:rows])
+
+    cb = mz.mosaic_chunk_cb(on_chunk)
+    for _ in range(2):
+        status = (ctypes.c_uint32 * n_chunks)(*([7] * n_chunks))
+        st = _noalloc(H, idx, W, out, chunk_rows=chunk, cb=cb, so=so, moff=moff, status=status)
+        assert st == mz.MOSAIC_OK, mz.mosaic_last_error_string()
+        assert list(status) == [0] * n_chunks
+        assert torch.equal(full.view(torch.int16), ref.view(torch.int16))
+    # mask_offsets[B] = M - 1 (not M): every access stays bounded (rows are resolved through the
+    # offsets and range-checked against their sequence), and the offsets check flags chunk 0
+    bad = moff.clone()
+    bad[-1] = M - 1
+    status = (ctypes.c_uint32 * n_chunks)(*([0] * n_chunks))
+    st = _noalloc(H, idx, W, out, chunk_rows=chunk, cb=cb, so=so, moff=bad, status=status)
+    assert st == mz.MOSAIC_ERR_INDEX
+    assert status[0] & 1 and all(w == 0 for w in list(status)[1:])
