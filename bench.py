@@ -50,6 +50,7 @@ def workload_set(name):
         "decode": [wl.DECODE],
         "dream": [wl.DREAM],
         "long": wl.LONG,
+        "dream_chunk": [wl.DREAM_CHUNK],
     }
     for w in wl.LONG + wl.LLADA:
         table[w.name] = [w]
@@ -92,16 +93,23 @@ MEASURED_TRAFFIC = {
     #     python bench.py --workload llada8b --no-graph --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
     # r_m 0.1 / 0.5 / 0.9 launches: 1.137 / 1.859 / 2.763 GB (mean per launch below)
     "efb394bd87f06b2b": {"llada8b": 1919696469},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+    #     -k regex:gather_gemm -s 66 -c 22 python bench.py --workload dream --no-graph --steps 1
+    #     --warmup 3 --no-e2e --no-cpu-baseline --no-cublas-context
+    # (one pass: the step's 22 launches at full size; mean 5.702 GB read + 2.359 GB written)
+    # and the same metrics plus time and L2 hit rate, -s 3 -c 1, on --workload dream_chunk.
+    "d725342dfd59cc0b": {"dream": 8061049961, "dream_chunk": 8523418112},
 }
 
 
-KERNEL_SOURCES = ("gather_gemm.cu", "gather_gemm.h", "ptx.cuh")
+# The device code, and the host code that sets its schedule (raster groups, grid).
+KERNEL_SOURCES = ("gather_gemm.cu", "gather_gemm.h", "ptx.cuh", "capi.cu")
 
 
 def kernel_source_hash():
     """sha256 over the code of the gather-GEMM kernel's sources (the device code whose DRAM
-    traffic the capture measured): `//` comments and blank lines are left out, so editing a
-    comment keeps the hash."""
+    traffic the capture measured, and the host code that picks its schedule): `//` comments and
+    blank lines are left out, so editing a comment keeps the hash."""
     import hashlib
     import re
 

@@ -175,5 +175,11 @@ LONG = [_w(f"long_L131072_r{r}_chunk4096", B=1, L=131072, d=4096, V=126464, out_
 DREAM = _w("dream7b_ragged_8x32768_chunk8192", B=8, L=32768, d=3584, V=152064, out_dtype="bf16",
            chunk_rows=8192, mask_kind="ragged", seed=1004)
 
+# One launch of the Dream-shaped batch's chunk size (8192 masked rows of d = 3584 against
+# V = 152,064), on hidden states small enough (65,536 rows) that a metric capture of it holds
+# about 4 GB on the device: a profiling case, not one of the five batch shapes.
+DREAM_CHUNK = _w("dream7b_chunk_L65536_M8192", B=1, L=65536, d=3584, V=152064, out_dtype="bf16",
+                 chunk_rows=0, mask_kind="flat", r_m=0.125, seed=1005)
+
 ALL = [TINY] + LLADA + [DECODE] + LONG + [DREAM]
 BY_NAME = {w.name: w for w in ALL}
