@@ -87,3 +87,13 @@ def test_fp8_long_context_chunked_equals_unchunked_and_oracle(mo):
     assert torch.equal(chunked.view(torch.int16), whole.view(torch.int16))
     del whole
     check(w, qH, sH, qW, sW, mask, chunked, seed=w.seed)
+
+
+def test_fp8_dream_shape_chunked_equals_unchunked_and_oracle(mo):
+    w = wl.DREAM     # ragged 8 x 32768, CSR, d = 3584, V = 152,064, chunks of 8192 rows
+    qH, sH, qW, sW, mask = quantized_inputs(w)
+    chunked = run(mo, w, qH, sH, qW, sW, mask, w.chunk_rows)
+    whole = run(mo, w, qH, sH, qW, sW, mask, 0)
+    assert torch.equal(chunked.view(torch.int16), whole.view(torch.int16))
+    del whole
+    check(w, qH, sH, qW, sW, mask, chunked, seed=w.seed)

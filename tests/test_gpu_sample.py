@@ -155,3 +155,36 @@ def test_sample_full_size_sampled_rows(mo, w):
     ri = np.sort(np.random.default_rng(w.seed).choice(mask.M, 48, replace=False))
     logits = orc.masked_logits(bits(H), rows[ri].astype(np.int32), bits(W))
     check_against_logits(token[torch.from_numpy(ri).to(DEV)], conf[torch.from_numpy(ri).to(DEV)], logits)
+
+
+def test_sample_full_size_every_row_llada_r05(mo):
+    """Every masked row of the LLaDA-8B r_m = 0.5 shape (M = 2048) against the oracle's logits."""
+    w = wl.LLADA[1]
+    H, W, mask = w.hidden(DEV), w.weight(DEV), w.mask().to(DEV)
+    token, conf = mo.masked_sample(H, mask.idx, W)
+    assert mo.check() == mz.MOSAIC_OK
+    rows = oracle_rows(mask, w.L_tot).astype(np.int32)
+    logits = orc.masked_logits(bits(H), rows, bits(W))
+    clear = check_against_logits(token, conf, logits)
+    assert clear > 0.8 * mask.M  # the exact-token comparison covers most rows
+
+
+def test_sample_dream_shape_chunked_equals_unchunked_and_oracle(mo):
+    """The Dream-shaped ragged batch (CSR, M = 172,201) sampled in the bench's chunks of 8192
+    rows equals the unchunked call bit for bit; sampled rows against the oracle."""
+    w = wl.DREAM
+    H, W, mask = w.hidden(DEV), w.weight(DEV), w.mask().to(DEV)
+    t1, c1 = mo.masked_sample(H, mask.idx, W, mask.seq_offsets, mask.mask_offsets,
+                              chunk_rows=w.chunk_rows)
+    t0, c0 = mo.masked_sample(H, mask.idx, W, mask.seq_offsets, mask.mask_offsets)
+    assert mo.check() == mz.MOSAIC_OK
+    assert torch.equal(t0, t1) and torch.equal(c0, c1)
+    rows = oracle_rows(mask, w.L_tot)
+    M = mask.M
+    # rows of every sequence (first and last rows included) and of every chunk boundary
+    ri = set(np.random.default_rng(w.seed).choice(M, 40, replace=False).tolist()) | {0, M - 1}
+    ri |= {b for b in range(0, M, w.chunk_rows)} | {min(M, b + w.chunk_rows) - 1 for b in range(0, M, w.chunk_rows)}
+    ri = np.array(sorted(ri))
+    logits = orc.masked_logits(bits(H), rows[ri].astype(np.int32), bits(W))
+    sel = torch.from_numpy(ri).to(DEV)
+    check_against_logits(t1[sel], c1[sel], logits)
