@@ -8,7 +8,7 @@ import torch
 from masked_token_lm_gb300 import mosaic as mz
 from masked_token_lm_gb300 import workloads as wl
 from oracle import mask_only_logits as orc
-from tests.parity_utils import TOL, as_f64, assert_close, bits
+from tests.parity_utils import as_f64, assert_close, bits
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")

@@ -9,7 +9,6 @@ This file is collected last so a failure here does not hide the other tests' res
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
