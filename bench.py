@@ -13,7 +13,9 @@ captured once into a CUDA graph and the timed steps replay it (``--no-graph``: d
                   [--mode logits|sample|fp8] [--oracle-timing]
 
 Other workloads (--workload): llada8b (the LLaDA-8B LM head, r_m = 0.1, 0.5, 0.9 back to back),
-decode (16 x 2048 block decode), long (L = 131,072, four mask ratios), tiny, or one member by name.
+decode (16 x 2048 block decode), long (L = 131,072, four mask ratios), tiny, dream_chunk (one
+Dream-shaped chunk launch, for profiling), llada8b_M<m> (the LLaDA-8B head with m masked rows),
+or one member by name.
 
 Under torchrun (N > 1) every rank computes its own batch (different seeds) with no collective
 on the data path; timing is the max over ranks ("weak" scaling).
@@ -41,8 +43,17 @@ DEFAULT_WORKLOAD = "dream"
 
 
 def workload_set(name):
+    import re
+
     from masked_token_lm_gb300 import workloads as wl
 
+    m = re.fullmatch(r"llada8b_M(\d+)", name)
+    if m:  # the LLaDA-8B LM head with exactly M masked rows (small-M sweeps)
+        M = int(m.group(1))
+        if not 1 <= M <= 4096:
+            raise SystemExit("llada8b_M<m> needs 1 <= m <= 4096")
+        return [wl.Workload(name=name, B=1, L=4096, d=4096, V=126464, out_dtype="bf16",
+                            chunk_rows=0, mask_kind="flat", r_m=M / 4096, seed=1001)]
     table = {
         "llada8b": wl.LLADA,
         "tiny": [wl.TINY],

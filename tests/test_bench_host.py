@@ -117,3 +117,9 @@ def test_roofline_uses_the_burst_peak_and_reports_the_sustained_fraction():
     small = bench.roofline_entry(2 * 16 * 126464 * 4096, bench.algorithmic_bytes(16, 126464, 4096, 2),
                                  1.8e-4, peaks, "logits")
     assert small["bound"] == "hbm" and small["unit"] == "GB/s" and small["peak"] == 6784.8
+
+
+def test_small_m_workloads_have_exactly_m_rows():
+    for m in (1, 16, 320, 410, 4096):
+        (w,) = bench.workload_set(f"llada8b_M{m}")
+        assert w.mask().M == m and (w.d, w.V, w.L) == (4096, 126464, 4096)
