@@ -588,9 +588,17 @@ def bench_e2e(args, mo, mz, calls, tot_flops, world, dev, stream):
     (e_ms,) = max_over_ranks([e_ms], dev)
     if mo.check() != mz.MOSAIC_OK:
         raise SystemExit(f"kernel status in the e2e leg: {mz.mosaic_last_error_string()}")
+    # What reached the host is the device-timed leg's result bit for bit: each member's pinned
+    # buffer holds its last chunk (or all rows), the device-timed leg's output buffer the same.
+    for c, ho in zip(calls, host_out):
+        n = launch_rows(c["mask"].M, c["w"].chunk_rows)[-1]
+        if not torch.equal(ho[:n].view(torch.int16) if ho.dtype == torch.bfloat16 else ho[:n],
+                           c["out"][:n].cpu().view(torch.int16) if ho.dtype == torch.bfloat16
+                           else c["out"][:n].cpu()):
+            raise SystemExit(f"e2e leg: logits read back for {c['w'].name} differ from the device result")
     return {"value": world * tot_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-            "steps": n_e2e,
+            "steps": n_e2e, "verified": "last chunk on the host equals the device result bitwise",
             "path": "pinned host -> Mosaic.masked_logits (C ABI) -> pinned host; chunks read back "
                     "through two device staging buffers into one reused pinned chunk buffer"}
 
