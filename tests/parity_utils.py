@@ -35,13 +35,12 @@ def oracle_rows(mask, L_tot):
     return orc.resolve_rows(mask.idx.cpu().numpy(), L_tot, so, mo)
 
 
-def sampled_parity(H_bits, W_bits, rows, get_rows, out_dtype, seed, n_rows=48, n_cols=384,
-                   must_rows=()):
-    """Compare sampled outputs with the oracle.
+def sampled_parity(H_bits, W_bits, rows, get_rows, out_dtype, seed, n_rows=48, must_rows=()):
+    """Compare sampled output rows with the oracle, all V columns of each.
 
     H_bits/W_bits: host uint16 patterns of the full inputs; rows: the oracle's resolved hidden
-    row per output row; get_rows(i_array) -> torch tensor [len(i), V] of GPU outputs;
-    also checks every output row on a seeded slice of columns (get_cols)."""
+    row per output row; get_rows(i_array) -> torch tensor [len(i), V] of GPU outputs. The rows are
+    n_rows seeded ones, the first and the last, and must_rows."""
     M = rows.shape[0]
     g = np.random.default_rng(seed)
     ri = set(g.choice(M, min(n_rows, M), replace=False).tolist()) | {0, M - 1} | set(must_rows)

@@ -3,8 +3,8 @@
 * The LLaDA-8B LM head at r_m = 0.1 / 0.5 / 0.9 and block decode: every element of the [M, V]
   output against the oracle (at most 3.8 TFLOP of fp64 on the host cores).
 * Long context and the Dream-shaped batch (up to 10^2 TFLOP, too large for the oracle to check
-  every element): sampled rows (all V columns) plus every row on a seeded slice of columns
-  against the oracle; the chunked call (the workload's chunk_rows) equals the unchunked call
+  every element): 256 sampled rows (all V columns, with the first and last row of every chunk)
+  plus every row on a seeded slice of 512 columns against the oracle; the chunked call (the workload's chunk_rows) equals the unchunked call
   bitwise; one-hot hidden states give out[i, v] == W[v, row(i) mod d] exactly, for every element.
 """
 import numpy as np
@@ -53,10 +53,12 @@ def check_against_oracle(w, H, mask, W, out, seed):
     if w.chunk_rows:
         for b in range(0, mask.M, w.chunk_rows):
             must += [b, min(mask.M, b + w.chunk_rows) - 1]
+    # 256 seeded rows against all V columns (plus the first and last row of every chunk), and
+    # every row on a seeded slice of 512 columns
     sampled_parity(Hb, Wb, rows, lambda ri: out[torch.from_numpy(ri).to(DEV)], torch.bfloat16
-                   if w.out_dtype == "bf16" else torch.float32, seed, must_rows=must)
+                   if w.out_dtype == "bf16" else torch.float32, seed, n_rows=256, must_rows=must)
     column_parity(Hb, Wb, rows, lambda cols: out[:, torch.from_numpy(cols).to(DEV)],
-                  torch.bfloat16 if w.out_dtype == "bf16" else torch.float32, seed)
+                  torch.bfloat16 if w.out_dtype == "bf16" else torch.float32, seed, n_cols=512)
 
 
 @pytest.mark.parametrize("w", wl.LLADA + [wl.DECODE], ids=lambda w: w.name)
