@@ -9,20 +9,25 @@
 // buffer is ever written. The pages' kernel targeted RTX 3090 / A100; this one is designed for
 // Blackwell instead.
 //
-// Roles (per CTA, 480 threads):
-//   warps 10..13 A gather: each of the 128 threads resolves 8 of the tile's mask indices to
-//               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
-//               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
-//               a 4-deep shared-memory ring (8 threads cover one 128-byte row segment).
-//   warp 14     relay: when a stage's gathered rows have landed, fences them into the async
-//               proxy and reports the stage to the (leader's) full barrier.
+// Roles (per CTA, 512 threads = 4 warpgroups; a warpgroup is 4 consecutive warps):
 //   warp 0      W stream: one thread issues the 2-D TMA loads of the W rows of each K block.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into two 256-column TMEM accumulator
 //               slots and commits stage releases.
-//   warps 2..9  epilogue, two warps per TMEM lane quadrant, each half of them taking 128
+//   warp 2      relay: when a stage's gathered rows have landed, fences them into the async
+//               proxy and reports the stage to the (leader's) full barrier.
+//   warp 3      idle after the prologue.
+//   warps 4..7  A gather: each of the 128 threads resolves 8 of the tile's mask indices to
+//               hidden rows (index staging, once per tile) and, per K block, copies one 16-byte
+//               piece of each of its 8 rows with cp.async into the 128-byte-swizzled A stage of
+//               a 4-deep shared-memory ring (8 threads cover one 128-byte row segment).
+//   warps 8..15 epilogue, two warps per TMEM lane quadrant, each half of them taking 128
 //               columns of a slot: tcgen05.ld the accumulator into registers (rounded to bf16),
 //               hand the slot back, then write 128-byte-swizzled staging tiles and TMA-store
 //               them; rows past the chunk are clipped by the store's tensor map.
+// The roles are grouped by warpgroup so that the kernels whose epilogue holds both slots of a
+// unit can move registers to it: right after the prologue, warpgroups 0-1 drop to REGS_LOW and
+// warpgroups 2-3 rise to REGS_HIGH registers per thread (setmaxnreg acts on a whole warpgroup,
+// each of whose warps executes the same instruction).
 //
 // PAIR = true (the normal case): two CTAs of a cluster form a pair that computes a 256 x 512
 // unit: per K step two tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), one per adjacent
@@ -34,7 +39,10 @@
 // CTAs (each CTA's cta_group::2 TMA load reports its bytes there), and each CTA's relay reports
 // its own gathered rows. Commits multicast to both CTAs. The slots are drained one after the
 // other; the MMA issuer starts the next unit's slot-0 MMAs while slot 1 is still being read,
-// holding up to 3 stages whose slot-1 MMAs it issues once that slot is free. PAIR = false runs
+// holding up to 3 stages whose slot-1 MMAs it issues once that slot is free. With bf16 output
+// the epilogue reads both slots (64 packed registers per panel and thread) and hands both back
+// before it stores either, so slot 1 returns after two slot reads instead of after slot 0's
+// stores; the stores then overlap the next unit's MMAs. PAIR = false runs
 // 128 x 256 tiles on one CTA (problems with a single M tile), alternating the two slots.
 //
 // The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
@@ -75,14 +83,28 @@ constexpr int EPI_BUFS = 2;           // one per epilogue half
 constexpr int TMEM_COLS = 2 * BN;     // two accumulator slots
 constexpr int STAGES = 4;
 constexpr int B_STAGE = 2 * 128 * BK * 2;  // 32 KiB of W rows per stage (both forms)
-constexpr int EPI_WARP0 = 2;
-constexpr int EPI_THREADS = 256;      // warps 2..9: two per TMEM lane quadrant
-constexpr int A_WARP0 = 10;
+constexpr int RELAY_WARP = 2;
+constexpr int A_WARP0 = 4;            // warpgroup 1
 constexpr int A_WARPS = 4;
 constexpr int A_THREADS = 32 * A_WARPS;
 constexpr int A_ROWS = BM * PIECES / A_THREADS;  // rows per gather thread (PIECES threads per row)
-constexpr int RELAY_WARP = A_WARP0 + A_WARPS;   // 14
-constexpr int NUM_THREADS = (RELAY_WARP + 1) * 32;  // 480
+constexpr int EPI_WARP0 = 8;          // warpgroups 2 and 3: two warps per TMEM lane quadrant
+constexpr int EPI_THREADS = 256;
+constexpr int NUM_THREADS = 512;
+// Registers per thread: REGS_LAUNCH at launch (the whole register file for one CTA of 512
+// threads); kernels whose epilogue holds both slots then move 64 per thread from the producer
+// warpgroups to the epilogue warpgroups.
+constexpr int REGS_LAUNCH = 65536 / NUM_THREADS;  // 128
+constexpr int REGS_LOW = 64;
+constexpr int REGS_HIGH = 192;
+static_assert(2 * 128 * REGS_LOW + 2 * 128 * REGS_HIGH <= NUM_THREADS * REGS_LAUNCH,
+              "register split exceeds the launch's register pool");
+static_assert(REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && REGS_LOW >= 24 && REGS_HIGH <= 256,
+              "setmaxnreg counts");
+// The epilogue holds both slots of a pair unit (and the registers are split) when it writes
+// bf16 logits: 2 panels x 128 columns x 2 B per thread fit in 64 + 64 registers.
+template <bool OUT_F32, bool PAIR, bool SAMPLE>
+constexpr bool kHoldBoth = PAIR && !SAMPLE && !OUT_F32;
 constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
 
 template <bool PAIR>
@@ -266,6 +288,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int BKE = FP8 ? ROW_BYTES : BK;   // elements per K block
   constexpr int EPP = FP8 ? 16 : 8;           // elements per 16-byte piece
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN) : C::IDESC;
+  constexpr bool HOLD = kHoldBoth<OUT_F32, PAIR, SAMPLE>;
   extern __shared__ uint8_t smem_raw[];
   Smem<PAIR> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -322,227 +345,233 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto full_c = [&](int s) { return PAIR ? mapa_shared(sm.full(s), 0) : sm.full(s); };
   auto tempty_c = [&](int j) { return PAIR ? mapa_shared(sm.tempty(j), 0) : sm.tempty(j); };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- W stream (TMA)
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int u = unit0; u < num_units; u += unit_stride) {
-        const Unit t = unit_of<PAIR>(u, rank, p);
-        if (t.nsub == 0) continue;
-        bool alive = true;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
-          if constexpr (PAIR) {
-            // Per panel, this CTA loads its 128-row half of the panel's 256 W rows. The leader
-            // expects the halves of both CTAs; each load lands in its own CTA's shared memory
-            // and reports its bytes to the leader's barrier.
-            if (leader) mbar_arrive_expect_tx(sm.full(stage), C::w_tx(t.nsub));
-            for (int j = 0; j < t.nsub; ++j)
-              tma_load_2d_pair(sm.b(stage, j), &tm_w, kb * BKE,
-                               (t.panel0 + j) * BN + rank * C::B_BOX_ROWS, full_c(stage), pol_w);
-          } else {
-            mbar_arrive_expect_tx(sm.full(stage), C::w_tx(1));
-            tma_load_2d(sm.b(stage), &tm_w, kb * BKE, t.panel0 * BN, sm.full(stage), pol_w);
+  if (warp < EPI_WARP0) {
+    // Producer warpgroups 0 and 1: every warp executes this one instruction, then the
+    // roles split.
+    if constexpr (HOLD) setmaxnreg_dec<REGS_LOW>();
+    if (warp == 0) {
+      // ---------------------------------------------------------------- W stream (TMA)
+      if (lane == 0) {
+        const uint64_t pol_w = policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int u = unit0; u < num_units; u += unit_stride) {
+          const Unit t = unit_of<PAIR>(u, rank, p);
+          if (t.nsub == 0) continue;
+          bool alive = true;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p)) { alive = false; break; }
+            if constexpr (PAIR) {
+              // Per panel, this CTA loads its 128-row half of the panel's 256 W rows. The leader
+              // expects the halves of both CTAs; each load lands in its own CTA's shared memory
+              // and reports its bytes to the leader's barrier.
+              if (leader) mbar_arrive_expect_tx(sm.full(stage), C::w_tx(t.nsub));
+              for (int j = 0; j < t.nsub; ++j)
+                tma_load_2d_pair(sm.b(stage, j), &tm_w, kb * BKE,
+                                 (t.panel0 + j) * BN + rank * C::B_BOX_ROWS, full_c(stage), pol_w);
+            } else {
+              mbar_arrive_expect_tx(sm.full(stage), C::w_tx(1));
+              tma_load_2d(sm.b(stage), &tm_w, kb * BKE, t.panel0 * BN, sm.full(stage), pol_w);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (!alive) break;
         }
-        if (!alive) break;
       }
-    }
-    __syncwarp();
-  } else if (warp >= A_WARP0 && warp < RELAY_WARP) {
-    // ---------------------------------------------------------------- A gather (cp.async)
-    // The gather warps' instruction stream is on the critical path (they issue every copy of
-    // the gathered rows), so the per-K-block work is kept to the copies themselves: addresses
-    // advance by a constant, destinations and byte counts are fixed per tile.
-    const int at = threadIdx.x - A_WARP0 * 32;    // 0 .. A_THREADS-1
-    const int chunk = at % PIECES;                // 16-byte piece of a row segment
-    const int row0 = at / PIECES;                 // rows row0 + ROW_STEP * j
-    constexpr int ROW_STEP = A_THREADS / PIECES;
-    const uint64_t pol_a = policy_evict_last();   // gathered rows are re-read by every N tile
-    const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
-    const int64_t row_bytes = static_cast<int64_t>(p.d) * (FP8 ? 1 : 2);
-    const int k_full = p.d / BKE;                 // K blocks with every piece inside d
-    const bool tail_in = chunk * EPP < p.d % BKE; // this piece in the partial last K block
-    // The swizzle of TMA and of the MMA descriptors: the piece index (address bits 4..) is
-    // XORed with address bits 7.. of the row start (64-byte rows: (row / 2) % 4; 128: row % 8).
-    uint32_t dst_off[A_ROWS];
-#pragma unroll
-    for (int j = 0; j < A_ROWS; ++j) {
-      const int r = row0 + ROW_STEP * j;
-      dst_off[j] = r * ROW_BYTES + ((chunk ^ ((r * ROW_BYTES >> 7) & (PIECES - 1))) << 4);
-    }
-    int stage = 0;
-    uint32_t phase = 0;
-    bool alive = true;
-    // Index staging, part 2: the mask indices of a tile are loaded one tile ahead (they land
-    // while the previous tile's K loop runs) and resolved to rows at the tile's start.
-    int32_t vnext[A_ROWS];
-    auto load_idx = [&](int u, int32_t (&v)[A_ROWS]) {
-      const Unit t = unit_of<PAIR>(u, rank, p);
+      __syncwarp();
+    } else if (warp >= A_WARP0 && warp < A_WARP0 + A_WARPS) {
+      // ---------------------------------------------------------------- A gather (cp.async)
+      // The gather warps' instruction stream is on the critical path (they issue every copy of
+      // the gathered rows), so the per-K-block work is kept to the copies themselves: addresses
+      // advance by a constant, destinations and byte counts are fixed per tile.
+      const int at = threadIdx.x - A_WARP0 * 32;    // 0 .. A_THREADS-1
+      const int chunk = at % PIECES;                // 16-byte piece of a row segment
+      const int row0 = at / PIECES;                 // rows row0 + ROW_STEP * j
+      constexpr int ROW_STEP = A_THREADS / PIECES;
+      const uint64_t pol_a = policy_evict_last();   // gathered rows are re-read by every N tile
+      const char* hbase = static_cast<const char*>(p.hidden) + chunk * 16;
+      const int64_t row_bytes = static_cast<int64_t>(p.d) * (FP8 ? 1 : 2);
+      const int k_full = p.d / BKE;                 // K blocks with every piece inside d
+      const bool tail_in = chunk * EPP < p.d % BKE; // this piece in the partial last K block
+      // The swizzle of TMA and of the MMA descriptors: the piece index (address bits 4..) is
+      // XORed with address bits 7.. of the row start (64-byte rows: (row / 2) % 4; 128: row % 8).
+      uint32_t dst_off[A_ROWS];
 #pragma unroll
       for (int j = 0; j < A_ROWS; ++j) {
-        const int r = t.m * BM + row0 + ROW_STEP * j;
-        v[j] = r < p.rows ? __ldg(p.idx + p.row_begin + r) : 0;
+        const int r = row0 + ROW_STEP * j;
+        dst_off[j] = r * ROW_BYTES + ((chunk ^ ((r * ROW_BYTES >> 7) & (PIECES - 1))) << 4);
       }
-    };
-    if (unit0 < num_units) load_idx(unit0, vnext);
-    for (int u = unit0; u < num_units && alive; u += unit_stride) {
-      const Unit tc = unit_of<PAIR>(u, rank, p);
-      int32_t v[A_ROWS];
-#pragma unroll
-      for (int j = 0; j < A_ROWS; ++j) v[j] = vnext[j];
-      if (u + unit_stride < num_units) load_idx(u + unit_stride, vnext);
-      if (tc.nsub == 0) continue;
-      // Rows past the chunk and rows with a bad index are zero-filled: 0 source bytes (no read)
-      // from row 0 of H, an address that stays inside H for every full K block.
-      const char* src[A_ROWS];
-      uint32_t bytes[A_ROWS];
-#pragma unroll
-      for (int j = 0; j < A_ROWS; ++j) {
-        const int r = tc.m * BM + row0 + ROW_STEP * j;
-        bool ok = false;
-        int32_t row = 0;
-        if (r < p.rows) row = resolve_row(p, offs, p.row_begin + r, v[j], ok);
-        src[j] = hbase + static_cast<int64_t>(row) * row_bytes;
-        bytes[j] = ok ? 16u : 0u;
-      }
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        int go = 1;
-        if (lane == 0) go = wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p) ? 1 : 0;
-        go = __shfl_sync(0xffffffffu, go, 0);
-        if (!go) { alive = false; break; }
-        const uint32_t a_stage = sm.a(stage);
-        if (kb < k_full) {
-#pragma unroll
-          for (int j = 0; j < A_ROWS; ++j) cp_async_16(a_stage + dst_off[j], src[j], bytes[j], pol_a);
-        } else {  // partial last K block: pieces past d are zero-filled, named at the start of H
-#pragma unroll
-          for (int j = 0; j < A_ROWS; ++j)
-            cp_async_16(a_stage + dst_off[j], tail_in ? src[j] : hbase, tail_in ? bytes[j] : 0u, pol_a);
-        }
-#pragma unroll
-        for (int j = 0; j < A_ROWS; ++j) src[j] += BK * 2;
-        // Publish without waiting: the arrive on afull happens when these copies have landed;
-        // the relay then fences them into the async proxy for the tensor cores.
-        cp_async_arrive_noinc(sm.afull(stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-      }
-    }
-    cp_async_wait<0>();
-  } else if (warp == RELAY_WARP) {
-    // ---------------------------------------------------------------- relay
-    if (lane == 0) {
-      // Once a stage's gathered rows have landed (every gather thread's hardware arrive on
-      // afull), fence them into the async proxy and report the stage: in the leader (or a single
-      // CTA) by a local arrive on full; in the peer of a pair through the async proxy, with a
-      // 16-byte shared-to-shared bulk copy whose complete_tx lands on the leader's full barrier
-      // (a cluster-scope release arrive instead cost ~0.8 us per K block). Keeping the fence
-      // here keeps it off the MMA issuer, the kernel's critical thread.
-      const uint32_t dst = PAIR ? mapa_shared(sm.signal_slot(), 0) : 0;
       int stage = 0;
       uint32_t phase = 0;
       bool alive = true;
-      for (int u = unit0; u < num_units && alive; u += unit_stride) {
-        if (unit_of<PAIR>(u, rank, p).nsub == 0) continue;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
-          fence_proxy_async_smem();
-          if (leader) mbar_arrive(sm.full(stage));
-          else bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && leader) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t tphase = 0;  // bit j: parity of the current use of accumulator slot j
-      int slot_next = 0;    // single CTA: tiles alternate between the two slots
-      bool alive = true;
-      bool issued_any = false;
-      // The 4 MMAs of one K block of panel j (W rows b(st, j)) into accumulator slot `slot`.
-      auto mma_kblock = [&](int st, int kb, int slot, int j) {
-        const uint64_t a0 = smem_desc_kmajor<ROW_BYTES>(sm.a(st));
-        const uint64_t b0 = smem_desc_kmajor<ROW_BYTES>(sm.b(st, j));
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
+      // Index staging, part 2: the mask indices of a tile are loaded one tile ahead (they land
+      // while the previous tile's K loop runs) and resolved to rows at the tile's start.
+      int32_t vnext[A_ROWS];
+      auto load_idx = [&](int u, int32_t (&v)[A_ROWS]) {
+        const Unit t = unit_of<PAIR>(u, rank, p);
 #pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k) {
-          // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
-          if constexpr (FP8)
-            tc_mma_e4m3<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
-          else
-            tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+        for (int j = 0; j < A_ROWS; ++j) {
+          const int r = t.m * BM + row0 + ROW_STEP * j;
+          v[j] = r < p.rows ? __ldg(p.idx + p.row_begin + r) : 0;
         }
       };
+      if (unit0 < num_units) load_idx(unit0, vnext);
       for (int u = unit0; u < num_units && alive; u += unit_stride) {
-        const Unit t = unit_of<PAIR>(u, rank, p);
-        if (t.nsub == 0) continue;
-        const int s0 = PAIR ? 0 : slot_next;
-        if (!PAIR) slot_next ^= 1;
-        if (!wait_phase<PAIR>(sm.tempty(s0), ((tphase >> s0) & 1u) ^ 1u, sm, p)) { alive = false; break; }
-        tc_fence_after();
-        // Two panels (pair): slot 1 may still be draining the previous unit's second panel. The
-        // slot-0 MMAs run ahead meanwhile, holding up to STAGES - 1 stages whose slot-1 MMAs are
-        // issued (oldest first) as soon as the slot is free.
-        const uint32_t s1_parity = ((tphase >> 1) & 1u) ^ 1u;
-        bool s1_free = t.nsub < 2;
-        int held = 0;
-        auto flush_held = [&](int kb_end) {
-          int hs = stage - held;
-          if (hs < 0) hs += STAGES;
-          for (int i = 0; i < held; ++i) {
-            mma_kblock(hs, kb_end - held + i, 1, 1);
-            tc_commit<PAIR>(sm.empty(hs));  // frees the stage once these MMAs have read it
-            if (++hs == STAGES) hs = 0;
-          }
-          held = 0;
-        };
+        const Unit tc = unit_of<PAIR>(u, rank, p);
+        int32_t v[A_ROWS];
+#pragma unroll
+        for (int j = 0; j < A_ROWS; ++j) v[j] = vnext[j];
+        if (u + unit_stride < num_units) load_idx(u + unit_stride, vnext);
+        if (tc.nsub == 0) continue;
+        // Rows past the chunk and rows with a bad index are zero-filled: 0 source bytes (no read)
+        // from row 0 of H, an address that stays inside H for every full K block.
+        const char* src[A_ROWS];
+        uint32_t bytes[A_ROWS];
+#pragma unroll
+        for (int j = 0; j < A_ROWS; ++j) {
+          const int r = tc.m * BM + row0 + ROW_STEP * j;
+          bool ok = false;
+          int32_t row = 0;
+          if (r < p.rows) row = resolve_row(p, offs, p.row_begin + r, v[j], ok);
+          src[j] = hbase + static_cast<int64_t>(row) * row_bytes;
+          bytes[j] = ok ? 16u : 0u;
+        }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
-          tc_fence_after();
-          mma_kblock(stage, kb, s0, 0);
-          issued_any = true;
-          if (!s1_free) {
-            if (held < STAGES - 1 && !mbar_test_wait_cluster(sm.tempty(1), s1_parity)) {
-              ++held;
-              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-              continue;
-            }
-            if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
-            tc_fence_after();
-            s1_free = true;
-            flush_held(kb);
+          int go = 1;
+          if (lane == 0) go = wait_phase<false>(sm.empty(stage), phase ^ 1u, sm, p) ? 1 : 0;
+          go = __shfl_sync(0xffffffffu, go, 0);
+          if (!go) { alive = false; break; }
+          const uint32_t a_stage = sm.a(stage);
+          if (kb < k_full) {
+#pragma unroll
+            for (int j = 0; j < A_ROWS; ++j) cp_async_16(a_stage + dst_off[j], src[j], bytes[j], pol_a);
+          } else {  // partial last K block: pieces past d are zero-filled, named at the start of H
+#pragma unroll
+            for (int j = 0; j < A_ROWS; ++j)
+              cp_async_16(a_stage + dst_off[j], tail_in ? src[j] : hbase, tail_in ? bytes[j] : 0u, pol_a);
           }
-          if (t.nsub == 2) mma_kblock(stage, kb, 1, 1);
-          tc_commit<PAIR>(sm.empty(stage));
+#pragma unroll
+          for (int j = 0; j < A_ROWS; ++j) src[j] += BK * 2;
+          // Publish without waiting: the arrive on afull happens when these copies have landed;
+          // the relay then fences them into the async proxy for the tensor cores.
+          cp_async_arrive_noinc(sm.afull(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!alive) break;
-        tc_commit<PAIR>(sm.tfull(s0));  // slot s0 complete
-        if (t.nsub == 2) {
-          if (!s1_free) {  // fewer K blocks than the stages the slot-0 MMAs may run ahead
-            if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
-            tc_fence_after();
-            flush_held(p.k_blocks);
+      }
+      cp_async_wait<0>();
+    } else if (warp == RELAY_WARP) {
+      // ---------------------------------------------------------------- relay
+      if (lane == 0) {
+        // Once a stage's gathered rows have landed (every gather thread's hardware arrive on
+        // afull), fence them into the async proxy and report the stage: in the leader (or a single
+        // CTA) by a local arrive on full; in the peer of a pair through the async proxy, with a
+        // 16-byte shared-to-shared bulk copy whose complete_tx lands on the leader's full barrier
+        // (a cluster-scope release arrive instead cost ~0.8 us per K block). Keeping the fence
+        // here keeps it off the MMA issuer, the kernel's critical thread.
+        const uint32_t dst = PAIR ? mapa_shared(sm.signal_slot(), 0) : 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool alive = true;
+        for (int u = unit0; u < num_units && alive; u += unit_stride) {
+          if (unit_of<PAIR>(u, rank, p).nsub == 0) continue;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_phase<false>(sm.afull(stage), phase, sm, p)) { alive = false; break; }
+            fence_proxy_async_smem();
+            if (leader) mbar_arrive(sm.full(stage));
+            else bulk_copy_s2s_cluster(dst, sm.signal_slot(), C::SIGNAL_BYTES, full_c(stage));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          tc_commit<PAIR>(sm.tfull(1));
         }
-        tphase ^= (1u << s0) | (t.nsub == 2 ? 2u : 0u);
       }
-      if (issued_any) {
-        // Completes when every MMA issued above (and the arrives it triggers) has finished.
-        tc_commit_local<PAIR>(sm.drain());
-        drain_wait(sm.drain(), 0);
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0 && leader) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t tphase = 0;  // bit j: parity of the current use of accumulator slot j
+        int slot_next = 0;    // single CTA: tiles alternate between the two slots
+        bool alive = true;
+        bool issued_any = false;
+        // The 4 MMAs of one K block of panel j (W rows b(st, j)) into accumulator slot `slot`.
+        auto mma_kblock = [&](int st, int kb, int slot, int j) {
+          const uint64_t a0 = smem_desc_kmajor<ROW_BYTES>(sm.a(st));
+          const uint64_t b0 = smem_desc_kmajor<ROW_BYTES>(sm.b(st, j));
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * BN);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // advance the start address by k * 16 elements * 2 B = 32 B (2 in 16-B units)
+            if constexpr (FP8)
+              tc_mma_e4m3<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+            else
+              tc_mma_bf16<PAIR>(d_tmem, a0 + 2 * k, b0 + 2 * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+          }
+        };
+        for (int u = unit0; u < num_units && alive; u += unit_stride) {
+          const Unit t = unit_of<PAIR>(u, rank, p);
+          if (t.nsub == 0) continue;
+          const int s0 = PAIR ? 0 : slot_next;
+          if (!PAIR) slot_next ^= 1;
+          if (!wait_phase<PAIR>(sm.tempty(s0), ((tphase >> s0) & 1u) ^ 1u, sm, p)) { alive = false; break; }
+          tc_fence_after();
+          // Two panels (pair): slot 1 may still be draining the previous unit's second panel. The
+          // slot-0 MMAs run ahead meanwhile, holding up to STAGES - 1 stages whose slot-1 MMAs are
+          // issued (oldest first) as soon as the slot is free.
+          const uint32_t s1_parity = ((tphase >> 1) & 1u) ^ 1u;
+          bool s1_free = t.nsub < 2;
+          int held = 0;
+          auto flush_held = [&](int kb_end) {
+            int hs = stage - held;
+            if (hs < 0) hs += STAGES;
+            for (int i = 0; i < held; ++i) {
+              mma_kblock(hs, kb_end - held + i, 1, 1);
+              tc_commit<PAIR>(sm.empty(hs));  // frees the stage once these MMAs have read it
+              if (++hs == STAGES) hs = 0;
+            }
+            held = 0;
+          };
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_phase<PAIR>(sm.full(stage), phase, sm, p)) { alive = false; break; }
+            tc_fence_after();
+            mma_kblock(stage, kb, s0, 0);
+            issued_any = true;
+            if (!s1_free) {
+              if (held < STAGES - 1 && !mbar_test_wait_cluster(sm.tempty(1), s1_parity)) {
+                ++held;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                continue;
+              }
+              if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
+              tc_fence_after();
+              s1_free = true;
+              flush_held(kb);
+            }
+            if (t.nsub == 2) mma_kblock(stage, kb, 1, 1);
+            tc_commit<PAIR>(sm.empty(stage));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          if (!alive) break;
+          tc_commit<PAIR>(sm.tfull(s0));  // slot s0 complete
+          if (t.nsub == 2) {
+            if (!s1_free) {  // fewer K blocks than the stages the slot-0 MMAs may run ahead
+              if (!wait_phase<PAIR>(sm.tempty(1), s1_parity, sm, p)) { alive = false; break; }
+              tc_fence_after();
+              flush_held(p.k_blocks);
+            }
+            tc_commit<PAIR>(sm.tfull(1));
+          }
+          tphase ^= (1u << s0) | (t.nsub == 2 ? 2u : 0u);
+        }
+        if (issued_any) {
+          // Completes when every MMA issued above (and the arrives it triggers) has finished.
+          tc_commit_local<PAIR>(sm.drain());
+          drain_wait(sm.drain(), 0);
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    if constexpr (HOLD) setmaxnreg_inc<REGS_HIGH>();  // epilogue warpgroups 2 and 3
     // ---------------------------------------------------------------- epilogue
     // Two warps per TMEM lane quadrant: warp w may read lanes 32 * (w % 4) .. + 31, and the
     // warps of half h = 0 / 1 take columns h * 128 .. + 127 of the accumulator slot. Each half
@@ -603,147 +632,205 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
         s4[0] = sa * w.x; s4[1] = sa * w.y; s4[2] = sa * w.z; s4[3] = sa * w.w;
       };
-      for (int jp = 0; jp < tc.nsub; ++jp) {
-        // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
-        const int slot = PAIR ? jp : slot_next;
-        if (!PAIR) slot_next ^= 1;
-        if (et == 0)
-          *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
-        __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
-        named_bar_sync(1, EPI_THREADS);
-        if (!*sm.epi_go()) { go = false; break; }
-        tc_fence_after();
-        tphase ^= 1u << slot;
+      // FP8 with bf16 out: W's column scales from column c0, applied to 64 rounded, packed
+      // values (a second bf16 rounding).
+      auto scale_cols = [&](uint32_t (&w32)[32], int c0) {
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+          const int c = c0 + 4 * g;
+          const float4 w = c < p.V ? __ldg(reinterpret_cast<const float4*>(p.b_scale + c))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          uint32_t& a = w32[2 * g];
+          uint32_t& b = w32[2 * g + 1];
+          a = pack_bf16x2(__uint_as_float(a << 16) * w.x, __uint_as_float(a & 0xffff0000u) * w.y);
+          b = pack_bf16x2(__uint_as_float(b << 16) * w.z, __uint_as_float(b & 0xffff0000u) * w.w);
+        }
+      };
+      if constexpr (HOLD) {
+        // bf16 out, CTA pair: both panels of the unit are read out of TMEM (rounded and packed,
+        // 64 registers per panel) and both slots handed back before any store, so the MMA
+        // issuer gets slot 1 back two slot reads after the unit's last MMA; the four stores
+        // below then overlap the next unit's MMAs. 8-column TMEM loads keep the live registers
+        // within REGS_HIGH.
+        uint32_t pk[2][2][32];
         const int col_h = half * (BN / 2);  // first slot column of this half
-        const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
-        const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
-        if constexpr (SAMPLE) {
-          // Sampling epilogue: this row's maximum, its first column and the sum of exp(x - max)
-          // over the half's valid columns (fp32 logits straight from TMEM), in two blocks of 64
-          // columns; the slot is handed back right after the second block's TMEM read, before
-          // its arithmetic. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per
-          // column. Columns past V are checked for only where a block reaches past V. The two
-          // halves of the row are then merged through shared memory.
-          constexpr float LOG2E = 1.4426950408889634f;
-          float m = -INFINITY, s = 0.0f;
-          int a = 0;
-          const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
-          uint32_t v[64];
-          auto load64 = [&](int c0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tmem_ld_32x32b_x16(t_acc + c0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(v + q * 16));
-            tmem_wait_ld();
-          };
-          auto block = [&](int c0) {
-            const bool inside = valid >= c0 + 64;
-            float bm = -INFINITY;
+        for (int jp = 0; jp < 2; ++jp) {
+          if (jp < tc.nsub && go) {
+            if (et == 0)
+              *sm.epi_go() = wait_phase<false>(sm.tfull(jp), (tphase >> jp) & 1u, sm, p) ? 1 : 0;
+            __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
+            named_bar_sync(1, EPI_THREADS);
+            if (!*sm.epi_go()) {
+              go = false;
+            } else {
+              tc_fence_after();
+              tphase ^= 1u << jp;
+              const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(jp * BN + col_h);
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[j]));
-            if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
-              int ba = 0;
+              for (int q = 0; q < 16; ++q) {
+                uint32_t v[8];
+                tmem_ld_32x32b_x8(t_acc + q * 8, v);
+                tmem_wait_ld();
 #pragma unroll
-              for (int j = 63; j >= 0; --j)
-                if (__uint_as_float(v[j]) == bm && (inside || c0 + j < valid)) ba = j;
-              s *= ex2_approx((m - bm) * LOG2E);
-              m = bm;
-              a = n0 + c0 + ba;
-            }
-            const float mL = m * LOG2E;
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (inside || c0 + j < valid) s += ex2_approx(fmaf(__uint_as_float(v[j]), LOG2E, -mL));
-          };
-          load64(0);
-          block(0);
-          load64(64);
-          release_slot(slot);
-          block(64);
-          float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);
-          float* xs = xm + BM;
-          int* xa = reinterpret_cast<int*>(xs + BM);
-          if (half == 1) { xm[row_in_tile] = m; xs[row_in_tile] = s; xa[row_in_tile] = a; }
-          named_bar_sync(1, EPI_THREADS);  // the exchange above before the reads below
-          if (half == 0) {
-            const float m1 = xm[row_in_tile], s1 = xs[row_in_tile];
-            const int a1 = xa[row_in_tile];
-            // columns of half 0 come first: an equal maximum keeps half 0's index
-            if (m1 > m) { s = s * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
-            else if (s1 > 0.0f) { s += s1 * ex2_approx((m1 - m) * LOG2E); }
-            if (r < p.rows && tc.m < p.m_tiles) {
-              const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
-              p.part_max[o] = m;
-              p.part_sum[o] = s;
-              p.part_arg[o] = ok ? a : -1;
+                for (int j = 0; j < 4; ++j) {
+                  if constexpr (FP8)  // the row's scale here; the columns' at the store
+                    pk[jp][q >> 3][(q & 7) * 4 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sa,
+                                                                  __uint_as_float(v[2 * j + 1]) * sa);
+                  else
+                    pk[jp][q >> 3][(q & 7) * 4 + j] =
+                        pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                }
+              }
+              release_slot(jp);
             }
           }
-        } else if constexpr (OUT_F32) {
-          // fp32 out: 4 chunks of 32 columns (128 B per row), the slot released after the last load
-          for (int c = 0; c < BN / 2 / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(t_acc + c * 32, v);
-            tmem_wait_ld();
-            if constexpr (FP8) {
+        }
+        if (!go) break;
 #pragma unroll
-              for (int g = 0; g < 8; ++g) {
-                float s4[4];
-                col_scales(n0 + c * 32 + 4 * g, s4);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  v[4 * g + e] = __float_as_uint(__uint_as_float(v[4 * g + e]) * s4[e]);
-              }
-            }
+        for (int jp = 0; jp < 2; ++jp) {
+          if (jp < tc.nsub) {
             if (!ok) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = 0u;
+              for (int j = 0; j < 32; ++j) { pk[jp][0][j] = 0u; pk[jp][1][j] = 0u; }
             }
-            if (c == BN / 2 / 32 - 1) release_slot(slot);
-            stage_store(v, n0 + c * 32, tc.m);
+            const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
+            if constexpr (FP8) scale_cols(pk[jp][0], n0);
+            stage_store(pk[jp][0], n0, tc.m);
+            if constexpr (FP8) scale_cols(pk[jp][1], n0 + 64);
+            stage_store(pk[jp][1], n0 + 64, tc.m);
           }
-        } else {
-          // bf16 out: the half's 128 columns go to registers (rounded and packed) before any
-          // store, so the slot is handed back after 4 TMEM loads rather than after the stores.
-          uint32_t packed[2][32];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(t_acc + q * 16, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if constexpr (FP8)  // the row's scale here; the columns' after the slot is free
-                packed[q >> 2][(q & 3) * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sa,
-                                                              __uint_as_float(v[2 * j + 1]) * sa);
-              else
-                packed[q >> 2][(q & 3) * 8 + j] =
-                    pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            }
-          }
-          release_slot(slot);
-          if (!ok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) { packed[0][j] = 0u; packed[1][j] = 0u; }
-          }
-          // FP8: W's column scales, applied to the rounded values (a second bf16 rounding)
-          auto scale_cols = [&](uint32_t (&w32)[32], int c0) {
-#pragma unroll
-            for (int g = 0; g < 16; ++g) {
-              const int c = c0 + 4 * g;
-              const float4 w = c < p.V ? __ldg(reinterpret_cast<const float4*>(p.b_scale + c))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-              uint32_t& a = w32[2 * g];
-              uint32_t& b = w32[2 * g + 1];
-              a = pack_bf16x2(__uint_as_float(a << 16) * w.x, __uint_as_float(a & 0xffff0000u) * w.y);
-              b = pack_bf16x2(__uint_as_float(b << 16) * w.z, __uint_as_float(b & 0xffff0000u) * w.w);
-            }
-          };
-          if constexpr (FP8) scale_cols(packed[0], n0);
-          stage_store(packed[0], n0, tc.m);
-          if constexpr (FP8) scale_cols(packed[1], n0 + 64);
-          stage_store(packed[1], n0 + 64, tc.m);
         }
-      }  // panels of the unit
+      } else {
+        for (int jp = 0; jp < tc.nsub; ++jp) {
+          // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
+          const int slot = PAIR ? jp : slot_next;
+          if (!PAIR) slot_next ^= 1;
+          if (et == 0)
+            *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
+          __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
+          named_bar_sync(1, EPI_THREADS);
+          if (!*sm.epi_go()) { go = false; break; }
+          tc_fence_after();
+          tphase ^= 1u << slot;
+          const int col_h = half * (BN / 2);  // first slot column of this half
+          const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
+          const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
+          if constexpr (SAMPLE) {
+            // Sampling epilogue: this row's maximum, its first column and the sum of exp(x - max)
+            // over the half's valid columns (fp32 logits straight from TMEM), in two blocks of 64
+            // columns; the slot is handed back right after the second block's TMEM read, before
+            // its arithmetic. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per
+            // column. Columns past V are checked for only where a block reaches past V. The two
+            // halves of the row are then merged through shared memory.
+            constexpr float LOG2E = 1.4426950408889634f;
+            float m = -INFINITY, s = 0.0f;
+            int a = 0;
+            const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
+            uint32_t v[64];
+            auto load64 = [&](int c0) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                tmem_ld_32x32b_x16(t_acc + c0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(v + q * 16));
+              tmem_wait_ld();
+            };
+            auto block = [&](int c0) {
+              const bool inside = valid >= c0 + 64;
+              float bm = -INFINITY;
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[j]));
+              if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
+                int ba = 0;
+#pragma unroll
+                for (int j = 63; j >= 0; --j)
+                  if (__uint_as_float(v[j]) == bm && (inside || c0 + j < valid)) ba = j;
+                s *= ex2_approx((m - bm) * LOG2E);
+                m = bm;
+                a = n0 + c0 + ba;
+              }
+              const float mL = m * LOG2E;
+#pragma unroll
+              for (int j = 0; j < 64; ++j)
+                if (inside || c0 + j < valid) s += ex2_approx(fmaf(__uint_as_float(v[j]), LOG2E, -mL));
+            };
+            load64(0);
+            block(0);
+            load64(64);
+            release_slot(slot);
+            block(64);
+            float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);
+            float* xs = xm + BM;
+            int* xa = reinterpret_cast<int*>(xs + BM);
+            if (half == 1) { xm[row_in_tile] = m; xs[row_in_tile] = s; xa[row_in_tile] = a; }
+            named_bar_sync(1, EPI_THREADS);  // the exchange above before the reads below
+            if (half == 0) {
+              const float m1 = xm[row_in_tile], s1 = xs[row_in_tile];
+              const int a1 = xa[row_in_tile];
+              // columns of half 0 come first: an equal maximum keeps half 0's index
+              if (m1 > m) { s = s * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
+              else if (s1 > 0.0f) { s += s1 * ex2_approx((m1 - m) * LOG2E); }
+              if (r < p.rows && tc.m < p.m_tiles) {
+                const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
+                p.part_max[o] = m;
+                p.part_sum[o] = s;
+                p.part_arg[o] = ok ? a : -1;
+              }
+            }
+          } else if constexpr (OUT_F32) {
+            // fp32 out: 4 chunks of 32 columns (128 B per row), the slot released after the last load
+            for (int c = 0; c < BN / 2 / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_acc + c * 32, v);
+              tmem_wait_ld();
+              if constexpr (FP8) {
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  float s4[4];
+                  col_scales(n0 + c * 32 + 4 * g, s4);
+#pragma unroll
+                  for (int e = 0; e < 4; ++e)
+                    v[4 * g + e] = __float_as_uint(__uint_as_float(v[4 * g + e]) * s4[e]);
+                }
+              }
+              if (!ok) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0u;
+              }
+              if (c == BN / 2 / 32 - 1) release_slot(slot);
+              stage_store(v, n0 + c * 32, tc.m);
+            }
+          } else {
+            // bf16 out: the half's 128 columns go to registers (rounded and packed) before any
+            // store, so the slot is handed back after 4 TMEM loads rather than after the stores.
+            uint32_t packed[2][32];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(t_acc + q * 16, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if constexpr (FP8)  // the row's scale here; the columns' after the slot is free
+                  packed[q >> 2][(q & 3) * 8 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sa,
+                                                                __uint_as_float(v[2 * j + 1]) * sa);
+                else
+                  packed[q >> 2][(q & 3) * 8 + j] =
+                      pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              }
+            }
+            release_slot(slot);
+            if (!ok) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) { packed[0][j] = 0u; packed[1][j] = 0u; }
+            }
+            if constexpr (FP8) scale_cols(packed[0], n0);
+            stage_store(packed[0], n0, tc.m);
+            if constexpr (FP8) scale_cols(packed[1], n0 + 64);
+            stage_store(packed[1], n0 + 64, tc.m);
+          }
+        }  // panels of the unit
+      }
     }
     if (gt == 0) bulk_wait_group_all();
     __syncwarp();
@@ -785,6 +872,15 @@ cudaError_t prepare_one(int* clusters) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<PAIR>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if constexpr (kHoldBoth<F32, PAIR, SAMPLE>) {
+    // The register split assumes exactly REGS_LAUNCH registers per thread at launch: with
+    // fewer, the epilogue's increase would wait for registers that never come free. Refuse.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gather_gemm_kernel<F32, PAIR, SAMPLE, FP8>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != REGS_LAUNCH || fa.maxThreadsPerBlock < NUM_THREADS)
+      return cudaErrorInvalidConfiguration;
+  }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config<F32, PAIR>((PAIR ? 2 : 1) * 64, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(clusters, gather_gemm_kernel<F32, PAIR, SAMPLE, FP8>,

@@ -199,6 +199,18 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   return p;
 }
 
+// Set this warp's register count to N per thread (a multiple of 8 in [24, 256]). Every warp of
+// a warpgroup must execute the same instruction, outside divergent code; the increase waits
+// until the decreases of other warpgroups have returned enough registers to the CTA's pool.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------------------ tcgen05
 
 // Allocate `NCOLS` TMEM columns (whole warp); the base address is written to smem at dst.
