@@ -109,6 +109,9 @@ MEASURED_TRAFFIC = {
     # (one pass: the step's 22 launches at full size; mean 5.702 GB read + 2.359 GB written)
     # and the same metrics plus time and L2 hit rate, -s 3 -c 1, on --workload dream_chunk.
     "d725342dfd59cc0b": {"dream": 8061049961, "dream_chunk": 8523418112},
+    # the same two captures on the 16-warp build with the register split
+    # (mean 5.752 GB read + 2.357 GB written per launch of the step)
+    "1d50d76c612cf313": {"dream": 8108922030, "dream_chunk": 8849310464},
 }
 
 
