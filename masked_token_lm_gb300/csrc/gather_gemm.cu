@@ -24,10 +24,10 @@
 //               columns of a slot: tcgen05.ld the accumulator into registers (rounded to bf16),
 //               hand the slot back, then write 128-byte-swizzled staging tiles and TMA-store
 //               them; rows past the chunk are clipped by the store's tensor map.
-// The roles are grouped by warpgroup so that the kernels whose epilogue holds both slots of a
-// unit can move registers to it: right after the prologue, warpgroups 0-1 drop to REGS_LOW and
-// warpgroups 2-3 rise to REGS_HIGH registers per thread (setmaxnreg acts on a whole warpgroup,
-// each of whose warps executes the same instruction).
+// The roles are grouped by warpgroup so that the pair kernels with bf16 output or sampling can
+// move registers to the epilogue: right after the prologue, warpgroups 0-1 drop to 64 (72 when
+// sampling) and warpgroups 2-3 rise to 192 (184) registers per thread (setmaxnreg acts on a
+// whole warpgroup, each of whose warps executes the same instruction).
 //
 // PAIR = true (the normal case): two CTAs of a cluster form a pair that computes a 256 x 512
 // unit: per K step two tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), one per adjacent
@@ -95,16 +95,27 @@ constexpr int NUM_THREADS = 512;
 // threads); kernels whose epilogue holds both slots then move 64 per thread from the producer
 // warpgroups to the epilogue warpgroups.
 constexpr int REGS_LAUNCH = 65536 / NUM_THREADS;  // 128
-constexpr int REGS_LOW = 64;
-constexpr int REGS_HIGH = 192;
-static_assert(2 * 128 * REGS_LOW + 2 * 128 * REGS_HIGH <= NUM_THREADS * REGS_LAUNCH,
-              "register split exceeds the launch's register pool");
-static_assert(REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && REGS_LOW >= 24 && REGS_HIGH <= 256,
-              "setmaxnreg counts");
+// Producers keep 64 (72 in the sampling kernel, whose gather code needs more to avoid spills);
+// the epilogue gets the rest of the pool.
+template <bool SAMPLE>
+constexpr int kRegsLow = SAMPLE ? 72 : 64;
+template <bool SAMPLE>
+constexpr int kRegsHigh = 2 * REGS_LAUNCH - kRegsLow<SAMPLE>;
+template <bool SAMPLE>
+constexpr bool regs_ok() {
+  return 2 * 128 * kRegsLow<SAMPLE> + 2 * 128 * kRegsHigh<SAMPLE> <= NUM_THREADS * REGS_LAUNCH &&
+         kRegsLow<SAMPLE> % 8 == 0 && kRegsHigh<SAMPLE> % 8 == 0 && kRegsLow<SAMPLE> >= 24 &&
+         kRegsHigh<SAMPLE> <= 256;
+}
+static_assert(regs_ok<false>() && regs_ok<true>(), "register split outside the launch's pool");
 // The epilogue holds both slots of a pair unit (and the registers are split) when it writes
-// bf16 logits: 2 panels x 128 columns x 2 B per thread fit in 64 + 64 registers.
+// bf16 logits: 2 panels x 128 columns x 2 B per thread fit in 64 + 64 registers. The sampling
+// epilogue of a pair takes the split too: it reads a whole slot (128 fp32 registers) before
+// handing it back and doing its arithmetic.
 template <bool OUT_F32, bool PAIR, bool SAMPLE>
 constexpr bool kHoldBoth = PAIR && !SAMPLE && !OUT_F32;
+template <bool OUT_F32, bool PAIR, bool SAMPLE>
+constexpr bool kRegSplit = PAIR && !OUT_F32;
 constexpr int OFFS_CAP = 129;  // CSR offsets staged in shared memory when B + 1 <= OFFS_CAP
 
 template <bool PAIR>
@@ -289,6 +300,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int EPP = FP8 ? 16 : 8;           // elements per 16-byte piece
   constexpr uint32_t IDESC = FP8 ? idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN) : C::IDESC;
   constexpr bool HOLD = kHoldBoth<OUT_F32, PAIR, SAMPLE>;
+  constexpr bool SPLIT = kRegSplit<OUT_F32, PAIR, SAMPLE>;
   extern __shared__ uint8_t smem_raw[];
   Smem<PAIR> sm;
   sm.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp < EPI_WARP0) {
     // Producer warpgroups 0 and 1: every warp executes this one instruction, then the
     // roles split.
-    if constexpr (HOLD) setmaxnreg_dec<REGS_LOW>();
+    if constexpr (SPLIT) setmaxnreg_dec<kRegsLow<SAMPLE>>();
     if (warp == 0) {
       // ---------------------------------------------------------------- W stream (TMA)
       if (lane == 0) {
@@ -571,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
     }
   } else {
-    if constexpr (HOLD) setmaxnreg_inc<REGS_HIGH>();  // epilogue warpgroups 2 and 3
+    if constexpr (SPLIT) setmaxnreg_inc<kRegsHigh<SAMPLE>>();  // epilogue warpgroups 2 and 3
     // ---------------------------------------------------------------- epilogue
     // Two warps per TMEM lane quadrant: warp w may read lanes 32 * (w % 4) .. + 31, and the
     // warps of half h = 0 / 1 take columns h * 128 .. + 127 of the accumulator slot. Each half
@@ -646,12 +658,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           b = pack_bf16x2(__uint_as_float(b << 16) * w.z, __uint_as_float(b & 0xffff0000u) * w.w);
         }
       };
-      if constexpr (HOLD) {
+      if constexpr (SAMPLE && PAIR) {
+        // Sampling epilogue of a pair: per panel, this row's maximum, its first column and the
+        // sum of exp(x - max) over the half's valid columns, from the fp32 accumulators. Each
+        // slot is read whole (128 registers) and handed back before its arithmetic; the two
+        // halves of the row are merged for both panels at the end of the unit, through shared
+        // memory. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per column.
+        // Columns past V are checked for only where a block of 64 reaches past V.
+        constexpr float LOG2E = 1.4426950408889634f;
+        const int col_h = half * (BN / 2);  // first slot column of this half
+        float pm[2], ps[2];
+        int pa[2];
+#pragma unroll
+        for (int jp = 0; jp < 2; ++jp) {
+          if (jp < tc.nsub && go) {
+            if (et == 0)
+              *sm.epi_go() = wait_phase<false>(sm.tfull(jp), (tphase >> jp) & 1u, sm, p) ? 1 : 0;
+            __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
+            named_bar_sync(1, EPI_THREADS);
+            if (!*sm.epi_go()) {
+              go = false;
+            } else {
+              tc_fence_after();
+              tphase ^= 1u << jp;
+              const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(jp * BN + col_h);
+              uint32_t v[128];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                tmem_ld_32x32b_x16(t_acc + q * 16, *reinterpret_cast<uint32_t(*)[16]>(v + q * 16));
+              tmem_wait_ld();
+              release_slot(jp);
+              const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
+              const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
+              float m = -INFINITY, sum = 0.0f;
+              int a = 0;
+#pragma unroll
+              for (int c0 = 0; c0 < 128; c0 += 64) {
+                const bool inside = valid >= c0 + 64;
+                float bm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                  if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[c0 + j]));
+                if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
+                  int ba = 0;
+#pragma unroll
+                  for (int j = 63; j >= 0; --j)
+                    if (__uint_as_float(v[c0 + j]) == bm && (inside || c0 + j < valid)) ba = j;
+                  sum *= ex2_approx((m - bm) * LOG2E);
+                  m = bm;
+                  a = n0 + c0 + ba;
+                }
+                const float mL = m * LOG2E;
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                  if (inside || c0 + j < valid)
+                    sum += ex2_approx(fmaf(__uint_as_float(v[c0 + j]), LOG2E, -mL));
+              }
+              pm[jp] = m;
+              ps[jp] = sum;
+              pa[jp] = a;
+            }
+          }
+        }
+        if (!go) break;
+        float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);  // [2][BM]
+        float* xs = xm + 2 * BM;
+        int* xa = reinterpret_cast<int*>(xs + 2 * BM);
+        if (half == 1) {
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            if (jp < tc.nsub) {
+              xm[jp * BM + row_in_tile] = pm[jp];
+              xs[jp * BM + row_in_tile] = ps[jp];
+              xa[jp * BM + row_in_tile] = pa[jp];
+            }
+          }
+        }
+        named_bar_sync(1, EPI_THREADS);  // the exchange above before the reads below
+        if (half == 0) {
+#pragma unroll
+          for (int jp = 0; jp < 2; ++jp) {
+            if (jp < tc.nsub) {
+              float m = pm[jp], sum = ps[jp];
+              int a = pa[jp];
+              const float m1 = xm[jp * BM + row_in_tile], s1 = xs[jp * BM + row_in_tile];
+              const int a1 = xa[jp * BM + row_in_tile];
+              // columns of half 0 come first: an equal maximum keeps half 0's index
+              if (m1 > m) { sum = sum * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
+              else if (s1 > 0.0f) { sum += s1 * ex2_approx((m1 - m) * LOG2E); }
+              if (r < p.rows && tc.m < p.m_tiles) {
+                const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
+                p.part_max[o] = m;
+                p.part_sum[o] = sum;
+                p.part_arg[o] = ok ? a : -1;
+              }
+            }
+          }
+        }
+      } else if constexpr (HOLD) {
         // bf16 out, CTA pair: both panels of the unit are read out of TMEM (rounded and packed,
         // 64 registers per panel) and both slots handed back before any store, so the MMA
         // issuer gets slot 1 back two slot reads after the unit's last MMA; the four stores
         // below then overlap the next unit's MMAs. 8-column TMEM loads keep the live registers
-        // within REGS_HIGH.
+        // within the epilogue's share (192).
         uint32_t pk[2][2][32];
         const int col_h = half * (BN / 2);  // first slot column of this half
 #pragma unroll
@@ -872,7 +981,7 @@ cudaError_t prepare_one(int* clusters) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<PAIR>::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if constexpr (kHoldBoth<F32, PAIR, SAMPLE>) {
+  if constexpr (kRegSplit<F32, PAIR, SAMPLE>) {
     // The register split assumes exactly REGS_LAUNCH registers per thread at launch: with
     // fewer, the epilogue's increase would wait for registers that never come free. Refuse.
     cudaFuncAttributes fa;
