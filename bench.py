@@ -112,6 +112,8 @@ MEASURED_TRAFFIC = {
     # the same two captures on the 16-warp build with the register split
     # (mean 5.752 GB read + 2.357 GB written per launch of the step)
     "1d50d76c612cf313": {"dream": 8108922030, "dream_chunk": 8849310464},
+    # and on the build whose sampling epilogue takes the split too (logits code unchanged)
+    "fb96857a8e98c3e5": {"dream": 7805993356, "dream_chunk": 8155889664},
 }
 
 
