@@ -617,6 +617,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bulk_commit_group();
       }
     };
+    // One epilogue thread waits (bounded) until accumulator slot `slot` holds a finished panel
+    // and tells the others through shared memory; false when the wait ran out.
+    auto acquire_slot = [&](int slot) -> bool {
+      if (et == 0)
+        *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
+      __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
+      named_bar_sync(1, EPI_THREADS);
+      if (!*sm.epi_go()) return false;
+      tc_fence_after();
+      tphase ^= 1u << slot;
+      return true;
+    };
     // All TMEM reads of the slot are done in every epilogue thread: hand it back to the MMA issuer.
     auto release_slot = [&](int slot) {
       tc_fence_before();
@@ -672,15 +684,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int jp = 0; jp < 2; ++jp) {
           if (jp < tc.nsub && go) {
-            if (et == 0)
-              *sm.epi_go() = wait_phase<false>(sm.tfull(jp), (tphase >> jp) & 1u, sm, p) ? 1 : 0;
-            __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
-            named_bar_sync(1, EPI_THREADS);
-            if (!*sm.epi_go()) {
+            if (!acquire_slot(jp)) {
               go = false;
             } else {
-              tc_fence_after();
-              tphase ^= 1u << jp;
               const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(jp * BN + col_h);
               uint32_t v[128];
 #pragma unroll
@@ -766,15 +772,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int jp = 0; jp < 2; ++jp) {
           if (jp < tc.nsub && go) {
-            if (et == 0)
-              *sm.epi_go() = wait_phase<false>(sm.tfull(jp), (tphase >> jp) & 1u, sm, p) ? 1 : 0;
-            __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
-            named_bar_sync(1, EPI_THREADS);
-            if (!*sm.epi_go()) {
+            if (!acquire_slot(jp)) {
               go = false;
             } else {
-              tc_fence_after();
-              tphase ^= 1u << jp;
               const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(jp * BN + col_h);
 #pragma unroll
               for (int q = 0; q < 16; ++q) {
@@ -815,13 +815,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // Panel jp of the unit sits in slot jp (pair) or in the tile's slot (single CTA).
           const int slot = PAIR ? jp : slot_next;
           if (!PAIR) slot_next ^= 1;
-          if (et == 0)
-            *sm.epi_go() = wait_phase<false>(sm.tfull(slot), (tphase >> slot) & 1u, sm, p) ? 1 : 0;
-          __syncwarp();  // lane 0 of this warp waited alone; the barrier below is warp-aligned
-          named_bar_sync(1, EPI_THREADS);
-          if (!*sm.epi_go()) { go = false; break; }
-          tc_fence_after();
-          tphase ^= 1u << slot;
+          if (!acquire_slot(slot)) { go = false; break; }
           const int col_h = half * (BN / 2);  // first slot column of this half
           const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
           const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
