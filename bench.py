@@ -114,6 +114,8 @@ MEASURED_TRAFFIC = {
     "1d50d76c612cf313": {"dream": 8108922030, "dream_chunk": 8849310464},
     # and on the build whose sampling epilogue takes the split too (logits code unchanged)
     "fb96857a8e98c3e5": {"dream": 7805993356, "dream_chunk": 8155889664},
+    # and on the same code with the epilogue's slot wait factored into one helper
+    "9ba26e04727a3cfd": {"dream": 8092198633, "dream_chunk": 8610032896},
 }
 
 
