@@ -65,7 +65,9 @@ typedef void (*mosaic_chunk_cb)(int64_t chunk, int64_t row_begin, int64_t rows, 
 /*
  * Create a handle bound to CUDA device `device` (made current by this call). The handle owns
  * one small device status word and the device properties used for launch sizing. Returns
- * MOSAIC_ERR_UNSUPPORTED on a device that is not sm_103, MOSAIC_ERR_CUDA if CUDA fails.
+ * MOSAIC_ERR_UNSUPPORTED on a device that is not sm_103, MOSAIC_ERR_CUDA if CUDA fails,
+ * including when a kernel that moves registers between its warpgroups was not built with
+ * exactly 128 registers per thread (checked here, before any launch).
  */
 MOSAIC_API mosaic_status mosaic_create(mosaic_handle** handle, int device);
 

@@ -169,7 +169,7 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
     }
     if (e != cudaSuccess) {
       delete h;
-      return cuda_fail(e, "kernel attributes / cluster occupancy");
+      return cuda_fail(e, "kernel attributes (registers per thread) / cluster occupancy");
     }
   }
   for (int pair = 0; pair < 2 && e == cudaSuccess; ++pair) {
@@ -183,7 +183,7 @@ mosaic_status mosaic_create(mosaic_handle** handle, int device) {
     }
   if (e != cudaSuccess) {
     delete h;
-    return cuda_fail(e, "sampling / FP8 kernel attributes, cluster occupancy");
+    return cuda_fail(e, "sampling / FP8 kernel attributes (registers per thread), cluster occupancy");
   }
   e = cudaMalloc(&h->d_status, 256);
   if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 256);
@@ -561,7 +561,7 @@ mosaic_status noalloc_setup(int device, NoallocDevice** out) {
     for (int f32 = 0; f32 < 2; ++f32)
       for (int pair = 0; pair < 2; ++pair) {
         e = mosaic::gather_gemm_prepare(f32 != 0, pair != 0, &nd.max_clusters[f32][pair]);
-        if (e != cudaSuccess) return cuda_fail(e, "kernel attributes / cluster occupancy");
+        if (e != cudaSuccess) return cuda_fail(e, "kernel attributes (registers per thread) / cluster occupancy");
         if (nd.max_clusters[f32][pair] < 1) return fail(MOSAIC_ERR_CUDA, "kernel cannot be resident");
       }
     void* ptr = nullptr;
