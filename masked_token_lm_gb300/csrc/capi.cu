@@ -561,7 +561,8 @@ mosaic_status noalloc_setup(int device, NoallocDevice** out) {
     for (int f32 = 0; f32 < 2; ++f32)
       for (int pair = 0; pair < 2; ++pair) {
         e = mosaic::gather_gemm_prepare(f32 != 0, pair != 0, &nd.max_clusters[f32][pair]);
-        if (e != cudaSuccess) return cuda_fail(e, "kernel attributes (registers per thread) / cluster occupancy");
+        if (e != cudaSuccess)
+          return cuda_fail(e, "kernel attributes (registers per thread) / cluster occupancy");
         if (nd.max_clusters[f32][pair] < 1) return fail(MOSAIC_ERR_CUDA, "kernel cannot be resident");
       }
     void* ptr = nullptr;
