@@ -221,6 +221,38 @@ def test_out_of_range_index_sets_status_and_zero_fills_row(mo):
     assert mo.check() == mz.MOSAIC_OK  # the status word was cleared
 
 
+@pytest.mark.parametrize("chunk_rows", [0, 200])
+def test_bad_indices_in_both_pair_tiles_bf16(mo, chunk_rows):
+    """The CTA-pair kernel with bf16 output (both accumulator slots read before any store):
+    bad rows in the first and in the ragged second M tile, next to a bad row in the last chunk,
+    come out as zeros with the status set; every other row matches the oracle."""
+    L, d, V = 700, 256, 1032
+    H, W = rand_inputs(L, d, V, seed=41)
+    rng = np.random.default_rng(41)
+    idx = rng.integers(0, L, size=300).astype(np.int32)
+    bad = [3, 130, 257, 299]  # CTA 0 / CTA 1 of tile 0, tile 1 (44 valid rows), the last row
+    idx[bad] = [L, -5, L + 1000, 2 ** 30]
+    idx_t = torch.from_numpy(idx).to(DEV)
+    if chunk_rows:
+        result = torch.empty((300, V), dtype=torch.bfloat16, device=DEV)
+
+        def on_chunk(c, rb, rows, out):
+            result[rb:rb + rows].copy_(out[:rows])
+
+        mo.masked_logits(H, idx_t, W, chunk_rows=chunk_rows, on_chunk=on_chunk)
+        out = result
+    else:
+        out = mo.masked_logits(H, idx_t, W)
+    assert mo.check() == mz.MOSAIC_ERR_INDEX
+    o = out.cpu()
+    for r in bad:
+        assert torch.all(o[r].view(torch.int16) == 0), r
+    good = np.setdiff1d(np.arange(300), bad)
+    ref = orc.masked_logits(bits(H), idx[good], bits(W))
+    assert_close(out[torch.from_numpy(good).to(DEV)], ref, torch.bfloat16, "valid rows next to bad ones")
+    assert mo.check() == mz.MOSAIC_OK
+
+
 def test_csr_local_index_past_its_sequence_is_flagged(mo):
     d, V = 64, 256
     H, W = rand_inputs(16, d, V, seed=2)
