@@ -34,7 +34,7 @@
 // 256-column panel, each into its own TMEM slot, issued by the leader CTA. Each CTA gathers its
 // own 128 A rows and loads its own 128-row half of each panel's W rows, so per K block an SM
 // takes in 16 KiB of gathered rows and 32 KiB of W for 2 x 2^22 FLOP: 48 bytes per tensor-core
-// cycle (a 256 x 256 unit needs 64 and measured ~81 % tensor-pipe busy; this form ~92 %).
+// cycle (a 256 x 256 unit needs 64 and measured ~81 % tensor-pipe busy; this form ~91 %).
 // The leader's stage barriers collect the whole pair: its W expect_tx covers the boxes of both
 // CTAs (each CTA's cta_group::2 TMA load reports its bytes there), and each CTA's relay reports
 // its own gathered rows. Commits multicast to both CTAs. The slots are drained one after the
@@ -42,8 +42,9 @@
 // holding up to 3 stages whose slot-1 MMAs it issues once that slot is free. With bf16 output
 // the epilogue reads both slots (64 packed registers per panel and thread) and hands both back
 // before it stores either, so slot 1 returns after two slot reads instead of after slot 0's
-// stores; the stores then overlap the next unit's MMAs. PAIR = false runs
-// 128 x 256 tiles on one CTA (problems with a single M tile), alternating the two slots.
+// stores; the stores then overlap the next unit's MMAs. The sampling epilogue likewise reads a
+// whole slot (128 fp32 registers) before its arithmetic. PAIR = false runs 128 x 256 tiles on
+// one CTA (problems with a single M tile), alternating the two slots.
 //
 // The A rows are gathered with cp.async rather than TMA tile::gather4: measured on GB300, the
 // 32 gather4 instructions a 128-row K block needs held the kernel to ~26 % of the tensor peak,
