@@ -310,6 +310,11 @@ def test_bounded_wait_timeout_reports_and_context_survives(mo):
     out = run(mo, H[:256], idx[:100] % 256, W[:1024], torch.float32)
     ref = orc.masked_logits(bits(H[:256]), (idx[:100] % 256).cpu().numpy(), bits(W[:1024]))
     assert_close(out, ref, torch.float32, "after timeout")
+    # the CTA-pair kernel with bf16 output (the one whose warpgroups trade registers) runs again
+    sub = idx[:300] % 256
+    out = run(mo, H[:256], sub, W[:1024], torch.bfloat16)
+    ref = orc.masked_logits(bits(H[:256]), sub.cpu().numpy(), bits(W[:1024]))
+    assert_close(out, ref, torch.bfloat16, "pair kernel after timeout")
 
 
 def test_min_chunk_rows_drives_a_chunked_call_within_budget(mo):

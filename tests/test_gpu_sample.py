@@ -188,3 +188,21 @@ def test_sample_dream_shape_chunked_equals_unchunked_and_oracle(mo):
     logits = orc.masked_logits(bits(H), rows[ri].astype(np.int32), bits(W))
     sel = torch.from_numpy(ri).to(DEV)
     check_against_logits(t1[sel], c1[sel], logits)
+
+
+def test_sample_timeout_reports_and_the_next_call_is_exact(mo):
+    """A bounded wait that runs out inside the sampling kernel of a CTA pair (the epilogue holds
+    a whole slot in registers) reports a timeout; the next call on the same context is exact."""
+    L, d, V, M = 2048, 1024, 8200, 700
+    H = wl.make_hidden(L, d, 51, DEV)
+    W = wl.make_weight(V, d, 52, DEV)
+    idx = wl.uniform_positions(L, M, seed=53).to(DEV)
+    mo.set_wait_timeout(0)  # every wait that is not already satisfied gives up at once
+    try:
+        mo.masked_sample(H, idx, W)
+        assert mo.check() == mz.MOSAIC_ERR_TIMEOUT
+    finally:
+        mo.set_wait_timeout(2_000_000_000)
+    token, conf = mo.masked_sample(H, idx, W)
+    assert mo.check() == mz.MOSAIC_OK
+    check_against_logits(token, conf, orc.masked_logits(bits(H), idx.cpu().numpy(), bits(W)))
