@@ -25,7 +25,7 @@ def compile_client(out_dir):
     cudalib = os.path.join(CUDA, "lib64")
     cmd = [cc, "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror",
            "-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include"), SRC,
-           "-o", exe, "-L", libdir, "-lmosaic", "-L", cudalib, "-lcudart",
+           "-o", exe, "-L", libdir, "-lmosaic", "-L", cudalib, "-lcudart", "-lm",
            f"-Wl,-rpath,{libdir}:{cudalib}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
@@ -42,3 +42,6 @@ def test_c_client_runs_exact(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "elements exact over 3 chunks" in r.stdout
+    for line in ("csr bf16: 312000 elements exact", "sampling: 300 tokens exact",
+                 "noalloc: bit for bit over 3 chunks", "min_chunk_rows: 100 x 3"):
+        assert line in r.stdout, r.stdout
