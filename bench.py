@@ -118,6 +118,8 @@ MEASURED_TRAFFIC = {
     "9ba26e04727a3cfd": {"dream": 8092198633, "dream_chunk": 8610032896},
     # and after an error-message change in capi.cu (the schedule and device code unchanged)
     "1202b6c212626a55": {"dream": 8340067025, "dream_chunk": 8525994240},
+    # and after the sampling epilogues' shared fold/merge helpers (the logits code unchanged)
+    "bfab402e17a4fe41": {"dream": 9608324201, "dream_chunk": 9778002432},
 }
 
 

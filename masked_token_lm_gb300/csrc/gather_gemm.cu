@@ -288,6 +288,48 @@ __device__ __forceinline__ Unit unit_of(int u, int rank, const GatherGemmParams&
   return t;
 }
 
+// Greedy-sampling fold of 64 fp32 logits v[off .. off + 63], the columns n0 + c0 + j of this
+// thread's row half (only those with c0 + j < valid count, unless the block lies inside V): the
+// running maximum m, its first column a and the sum s of exp(x - m), rescaled when the maximum
+// grows. exp(x - m) = 2^(x log2(e) - m log2(e)): one FMA and one ex2 per column.
+constexpr float SAMPLE_LOG2E = 1.4426950408889634f;
+template <int N>
+__device__ __forceinline__ void sample_fold64(const uint32_t (&v)[N], int off, int c0, int valid,
+                                              int n0, float& m, float& s, int& a) {
+  const bool inside = valid >= c0 + 64;
+  float bm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 64; ++j)
+    if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[off + j]));
+  if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
+    int ba = 0;
+#pragma unroll
+    for (int j = 63; j >= 0; --j)
+      if (__uint_as_float(v[off + j]) == bm && (inside || c0 + j < valid)) ba = j;
+    s *= ex2_approx((m - bm) * SAMPLE_LOG2E);
+    m = bm;
+    a = n0 + c0 + ba;
+  }
+  const float mL = m * SAMPLE_LOG2E;
+#pragma unroll
+  for (int j = 0; j < 64; ++j)
+    if (inside || c0 + j < valid)
+      s += ex2_approx(fmaf(__uint_as_float(v[off + j]), SAMPLE_LOG2E, -mL));
+}
+
+// Merge the other row half's (m1, s1, a1) into this half's (m, s, a). This half's columns come
+// first, so an equal maximum keeps its index.
+__device__ __forceinline__ void sample_merge(float& m, float& s, int& a, float m1, float s1,
+                                             int a1) {
+  if (m1 > m) {
+    s = s * ex2_approx((m - m1) * SAMPLE_LOG2E) + s1;
+    m = m1;
+    a = a1;
+  } else if (s1 > 0.0f) {
+    s += s1 * ex2_approx((m1 - m) * SAMPLE_LOG2E);
+  }
+}
+
 // FP8: E4M3 operands (per-row scales applied in the epilogue): a K block is then 128 elements of
 // the same 128-byte rows, and the MMA is kind::f8f6f4 (K = 32 per instruction, 4 per K block).
 template <bool OUT_F32, bool PAIR, bool SAMPLE, bool FP8 = false>
@@ -676,9 +718,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // sum of exp(x - max) over the half's valid columns, from the fp32 accumulators. Each
         // slot is read whole (128 registers) and handed back before its arithmetic; the two
         // halves of the row are merged for both panels at the end of the unit, through shared
-        // memory. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per column.
-        // Columns past V are checked for only where a block of 64 reaches past V.
-        constexpr float LOG2E = 1.4426950408889634f;
+        // memory.
         const int col_h = half * (BN / 2);  // first slot column of this half
         float pm[2], ps[2];
         int pa[2];
@@ -699,28 +739,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
               float m = -INFINITY, sum = 0.0f;
               int a = 0;
-#pragma unroll
-              for (int c0 = 0; c0 < 128; c0 += 64) {
-                const bool inside = valid >= c0 + 64;
-                float bm = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                  if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[c0 + j]));
-                if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
-                  int ba = 0;
-#pragma unroll
-                  for (int j = 63; j >= 0; --j)
-                    if (__uint_as_float(v[c0 + j]) == bm && (inside || c0 + j < valid)) ba = j;
-                  sum *= ex2_approx((m - bm) * LOG2E);
-                  m = bm;
-                  a = n0 + c0 + ba;
-                }
-                const float mL = m * LOG2E;
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                  if (inside || c0 + j < valid)
-                    sum += ex2_approx(fmaf(__uint_as_float(v[c0 + j]), LOG2E, -mL));
-              }
+              sample_fold64(v, 0, 0, valid, n0, m, sum, a);
+              sample_fold64(v, 64, 64, valid, n0, m, sum, a);
               pm[jp] = m;
               ps[jp] = sum;
               pa[jp] = a;
@@ -748,11 +768,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (jp < tc.nsub) {
               float m = pm[jp], sum = ps[jp];
               int a = pa[jp];
-              const float m1 = xm[jp * BM + row_in_tile], s1 = xs[jp * BM + row_in_tile];
-              const int a1 = xa[jp * BM + row_in_tile];
-              // columns of half 0 come first: an equal maximum keeps half 0's index
-              if (m1 > m) { sum = sum * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
-              else if (s1 > 0.0f) { sum += s1 * ex2_approx((m1 - m) * LOG2E); }
+              sample_merge(m, sum, a, xm[jp * BM + row_in_tile], xs[jp * BM + row_in_tile],
+                           xa[jp * BM + row_in_tile]);
               if (r < p.rows && tc.m < p.m_tiles) {
                 const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
                 p.part_max[o] = m;
@@ -821,13 +838,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t t_acc = tmem_base + lane_base + static_cast<uint32_t>(slot * BN + col_h);
           const int n0 = tc.panel0 * BN + jp * BN + col_h;  // first output column of this half
           if constexpr (SAMPLE) {
-            // Sampling epilogue: this row's maximum, its first column and the sum of exp(x - max)
-            // over the half's valid columns (fp32 logits straight from TMEM), in two blocks of 64
-            // columns; the slot is handed back right after the second block's TMEM read, before
-            // its arithmetic. exp(x - max) = 2^(x log2(e) - max log2(e)): one FMA and one ex2 per
-            // column. Columns past V are checked for only where a block reaches past V. The two
-            // halves of the row are then merged through shared memory.
-            constexpr float LOG2E = 1.4426950408889634f;
+            // Sampling epilogue of a single CTA: this row's maximum, its first column and the sum
+            // of exp(x - max) over the half's valid columns (fp32 logits straight from TMEM), in
+            // two blocks of 64 columns; the slot is handed back right after the second block's
+            // TMEM read, before its arithmetic. The two halves of the row are then merged through
+            // shared memory.
             float m = -INFINITY, s = 0.0f;
             int a = 0;
             const int valid = p.V - n0;  // columns of this half inside V (all when >= 128)
@@ -838,42 +853,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tmem_ld_32x32b_x16(t_acc + c0 + q * 16, *reinterpret_cast<uint32_t(*)[16]>(v + q * 16));
               tmem_wait_ld();
             };
-            auto block = [&](int c0) {
-              const bool inside = valid >= c0 + 64;
-              float bm = -INFINITY;
-#pragma unroll
-              for (int j = 0; j < 64; ++j)
-                if (inside || c0 + j < valid) bm = fmaxf(bm, __uint_as_float(v[j]));
-              if (bm > m) {  // a new maximum: its first column, and the sum rescaled to it
-                int ba = 0;
-#pragma unroll
-                for (int j = 63; j >= 0; --j)
-                  if (__uint_as_float(v[j]) == bm && (inside || c0 + j < valid)) ba = j;
-                s *= ex2_approx((m - bm) * LOG2E);
-                m = bm;
-                a = n0 + c0 + ba;
-              }
-              const float mL = m * LOG2E;
-#pragma unroll
-              for (int j = 0; j < 64; ++j)
-                if (inside || c0 + j < valid) s += ex2_approx(fmaf(__uint_as_float(v[j]), LOG2E, -mL));
-            };
             load64(0);
-            block(0);
+            sample_fold64(v, 0, 0, valid, n0, m, s, a);
             load64(64);
             release_slot(slot);
-            block(64);
+            sample_fold64(v, 0, 64, valid, n0, m, s, a);
             float* xm = reinterpret_cast<float*>(sm.base + Cfg<PAIR>::SMEM_EPI_OFF);
             float* xs = xm + BM;
             int* xa = reinterpret_cast<int*>(xs + BM);
             if (half == 1) { xm[row_in_tile] = m; xs[row_in_tile] = s; xa[row_in_tile] = a; }
             named_bar_sync(1, EPI_THREADS);  // the exchange above before the reads below
             if (half == 0) {
-              const float m1 = xm[row_in_tile], s1 = xs[row_in_tile];
-              const int a1 = xa[row_in_tile];
-              // columns of half 0 come first: an equal maximum keeps half 0's index
-              if (m1 > m) { s = s * ex2_approx((m - m1) * LOG2E) + s1; m = m1; a = a1; }
-              else if (s1 > 0.0f) { s += s1 * ex2_approx((m1 - m) * LOG2E); }
+              sample_merge(m, s, a, xm[row_in_tile], xs[row_in_tile], xa[row_in_tile]);
               if (r < p.rows && tc.m < p.m_tiles) {
                 const int64_t o = static_cast<int64_t>(r) * p.part_ld + tc.panel0 + jp;
                 p.part_max[o] = m;
